@@ -1,0 +1,309 @@
+"""GB300-native paged KV cache attention: Python binding of libpkv.
+
+The functions here only marshal torch tensors into the C ABI of
+``include/pkv.h`` (pointers, sizes, the current CUDA stream); every step of
+the path runs in libpkv's CUDA kernels or its C++ allocator.  There is no CPU
+or PyTorch fallback: a missing library or a non-CUDA tensor is an error.
+
+Calls (names as in the C ABI, without the ``pkv_`` prefix):
+
+* :func:`write_kv` -- scatter new K/V rows into their slots;
+* :func:`attn_decode` -- one query row per sequence over its paged keys;
+* :func:`attn_varlen` -- packed prefill chunks and decode rows, causal offset;
+* :func:`copy_blocks` -- block copies for copy-on-write;
+* :class:`BlockAllocator` -- host allocator producing tables, slots and pairs.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+from ._native import (DEVERR, PKV_BF16, PKV_F16, PKV_F32, DoubleFreeError, ExhaustedError, PkvCache,
+                      PkvCounters, PkvError, check, lib, library_path)
+
+__all__ = [
+    "write_kv", "attn_decode", "attn_varlen", "copy_blocks", "decode_workspace_size",
+    "varlen_workspace_size", "check_copy_pairs", "BlockAllocator", "PkvError", "ExhaustedError",
+    "DoubleFreeError", "DEVERR", "library_path",
+]
+
+_DT = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16, torch.float32: PKV_F32}
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cuda(t: torch.Tensor, name: str) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _cache(k_cache: torch.Tensor, v_cache: torch.Tensor) -> PkvCache:
+    _cuda(k_cache, "k_cache")
+    _cuda(v_cache, "v_cache")
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must both be [num_blocks, block_size, kv_heads, head_dim]")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous")
+    if k_cache.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("caches must be float16 or bfloat16")
+    nb, bs, hkv, d = k_cache.shape
+    return PkvCache(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, hkv, d, _DT[k_cache.dtype])
+
+
+def _row_stride(t: torch.Tensor, name: str) -> int:
+    """Elements between rows of a [rows, heads, dim] tensor with heads/dims packed."""
+    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError(f"{name} must be [rows, heads, head_dim] with heads and dims contiguous")
+    return t.stride(0)
+
+
+def _check_i32(t: torch.Tensor, name: str) -> None:
+    _cuda(t, name)
+    if t.dtype != torch.int32 or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous int32 CUDA tensor")
+
+
+def write_kv(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+             v_cache: torch.Tensor, err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Rows k[t], v[t] ([T, Hkv, D]) go to slot slot_mapping[t] (int64; < 0 skips)."""
+    c = _cache(k_cache, v_cache)
+    _cuda(k, "k")
+    _cuda(v, "v")
+    _cuda(slot_mapping, "slot_mapping")
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_contiguous():
+        raise TypeError("slot_mapping must be contiguous int64")
+    if k.shape != v.shape or k.dtype != k_cache.dtype or v.dtype != k_cache.dtype or k.stride() != v.stride():
+        raise ValueError("k and v must match each other and the cache dtype")
+    if k.shape[1:] != k_cache.shape[2:] or k.shape[0] != slot_mapping.numel():
+        raise ValueError("k is [T, kv_heads, head_dim] with T = slot_mapping.numel()")
+    check(lib().pkv_write_kv(_ptr(k), _ptr(v), _row_stride(k, "k"), _ptr(slot_mapping), k.shape[0],
+                             ctypes.byref(c), _ptr(err), _stream(stream)))
+
+
+def decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                          device: Optional[int] = None) -> int:
+    n = ctypes.c_size_t(0)
+    dev = torch.cuda.current_device() if device is None else device
+    check(lib().pkv_attn_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, dev,
+                                               ctypes.byref(n)))
+    return n.value
+
+
+def varlen_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                          device: Optional[int] = None) -> int:
+    n = ctypes.c_size_t(0)
+    dev = torch.cuda.current_device() if device is None else device
+    check(lib().pkv_attn_varlen_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, dev,
+                                               ctypes.byref(n)))
+    return n.value
+
+
+def _workspace(nbytes: int, workspace: Optional[torch.Tensor], device) -> torch.Tensor:
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError(f"workspace smaller than the {nbytes} bytes needed")
+        return workspace
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+
+
+def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                seq_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+                out_dtype: torch.dtype = torch.float32, workspace: Optional[torch.Tensor] = None,
+                err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """q [B, Hq, D]; tables [B, max_blocks] int32; seq_lens [B] int32 -> out [B, Hq, D]."""
+    c = _cache(k_cache, v_cache)
+    _cuda(q, "q")
+    _check_i32(block_tables, "block_tables")
+    _check_i32(seq_lens, "seq_lens")
+    if q.dtype != k_cache.dtype:
+        raise TypeError("q must have the cache dtype")
+    B, hq, d = q.shape
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
+    elif not out.is_contiguous() or out.shape != q.shape:
+        raise ValueError("out must be contiguous [B, Hq, D]")
+    ws = _workspace(decode_workspace_size(B, hq, c.num_kv_heads, d, q.device.index), workspace, q.device)
+    check(lib().pkv_attn_decode(_ptr(q), _row_stride(q, "q"), ctypes.byref(c), _ptr(block_tables),
+                                block_tables.shape[1] if block_tables.dim() == 2 else 0, _ptr(seq_lens), B, hq,
+                                float(scale), _ptr(out), _DT[out.dtype], _ptr(ws),
+                                ws.numel() * ws.element_size(), _ptr(err), _stream(stream)))
+    return out
+
+
+def attn_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                cu_seqlens_q: torch.Tensor, seq_lens: torch.Tensor, max_q_len: int, scale: float,
+                causal: bool = True, out: Optional[torch.Tensor] = None,
+                out_dtype: torch.dtype = torch.float32, workspace: Optional[torch.Tensor] = None,
+                err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Packed rows q [total_q, Hq, D]; cu_seqlens_q [B+1]; seq_lens = kv_len [B]."""
+    c = _cache(k_cache, v_cache)
+    _cuda(q, "q")
+    _check_i32(block_tables, "block_tables")
+    _check_i32(seq_lens, "seq_lens")
+    _check_i32(cu_seqlens_q, "cu_seqlens_q")
+    if q.dtype != k_cache.dtype:
+        raise TypeError("q must have the cache dtype")
+    total, hq, d = q.shape
+    B = seq_lens.numel()
+    if cu_seqlens_q.numel() != B + 1:
+        raise ValueError("cu_seqlens_q must have num_seqs + 1 entries")
+    if out is None:
+        out = torch.empty((total, hq, d), dtype=out_dtype, device=q.device)
+    ws = _workspace(varlen_workspace_size(B, hq, c.num_kv_heads, d, q.device.index), workspace, q.device)
+    check(lib().pkv_attn_varlen(_ptr(q), _row_stride(q, "q"), ctypes.byref(c), _ptr(block_tables),
+                                block_tables.shape[1], _ptr(cu_seqlens_q), _ptr(seq_lens), B, total,
+                                int(max_q_len), hq, float(scale), 1 if causal else 0, _ptr(out), _DT[out.dtype],
+                                _ptr(ws), ws.numel() * ws.element_size(), _ptr(err), _stream(stream)))
+    return out
+
+
+def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor], src_dst_pairs: torch.Tensor,
+                err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """For each (src, dst) row of src_dst_pairs (int64 [N, 2], CUDA): block dst <- block src, every layer."""
+    if len(k_caches) != len(v_caches):
+        raise ValueError("one v cache per k cache")
+    _cuda(src_dst_pairs, "src_dst_pairs")
+    if src_dst_pairs.dtype != torch.int64 or not src_dst_pairs.is_contiguous():
+        raise TypeError("src_dst_pairs must be contiguous int64")
+    arr = (PkvCache * max(1, len(k_caches)))(*[_cache(k, v) for k, v in zip(k_caches, v_caches)])
+    n = src_dst_pairs.numel() // 2
+    check(lib().pkv_copy_blocks(arr, len(k_caches), _ptr(src_dst_pairs), n, _ptr(err), _stream(stream)))
+
+
+def check_copy_pairs(pairs: Sequence[Tuple[int, int]], num_blocks: int) -> None:
+    flat = [int(x) for p in pairs for x in p]
+    buf = (ctypes.c_int64 * max(1, len(flat)))(*flat)
+    check(lib().pkv_check_copy_pairs(buf, len(flat) // 2, num_blocks))
+
+
+class BlockAllocator:
+    """Host block allocator and block tables (C++, behind the C ABI)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        h = ctypes.c_void_p()
+        check(lib().pkv_alloc_create(num_blocks, block_size, ctypes.byref(h)))
+        self._h = h
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            lib().pkv_alloc_destroy(h)
+            self._h = None
+
+    # block level
+    @property
+    def num_free(self) -> int:
+        return lib().pkv_alloc_num_free(self._h)
+
+    def set_free_order(self, order: Sequence[int]) -> None:
+        buf = (ctypes.c_int32 * max(1, len(order)))(*order)
+        check(lib().pkv_alloc_set_free_order(self._h, buf, len(order)))
+
+    def allocate(self) -> int:
+        out = ctypes.c_int32()
+        check(lib().pkv_alloc_allocate(self._h, ctypes.byref(out)))
+        return out.value
+
+    def blocks_needed(self, num_tokens: int) -> int:
+        n = lib().pkv_alloc_blocks_needed(self._h, num_tokens)
+        if n < 0:
+            raise ValueError("negative token count")
+        return n
+
+    def allocate_for(self, num_tokens: int) -> List[int]:
+        cap = max(1, self.blocks_needed(num_tokens)) if num_tokens >= 0 else 1
+        buf = (ctypes.c_int32 * cap)()
+        n = ctypes.c_int32()
+        check(lib().pkv_alloc_allocate_for(self._h, num_tokens, buf, cap, ctypes.byref(n)))
+        return list(buf[:n.value])
+
+    def free(self, block_id: int) -> None:
+        check(lib().pkv_alloc_free(self._h, block_id))
+
+    release = free
+
+    def free_all(self, ids: Sequence[int]) -> None:
+        buf = (ctypes.c_int32 * max(1, len(ids)))(*ids)
+        check(lib().pkv_alloc_free_all(self._h, buf, len(ids)))
+
+    def retain(self, block_id: int) -> None:
+        check(lib().pkv_alloc_retain(self._h, block_id))
+
+    def refcount(self, block_id: int) -> int:
+        return lib().pkv_alloc_refcount(self._h, block_id)
+
+    def counters(self) -> dict:
+        c = PkvCounters()
+        check(lib().pkv_alloc_counters_get(self._h, ctypes.byref(c)))
+        return {"allocs": c.allocs, "frees": c.frees, "cow_copies": c.cow_copies, "peak_used": c.peak_used}
+
+    # sequence level
+    def create_sequence(self, shared_ids: Sequence[int] = (), shared_tokens: int = 0) -> int:
+        buf = (ctypes.c_int32 * max(1, len(shared_ids)))(*shared_ids)
+        out = ctypes.c_int32()
+        check(lib().pkv_seq_create(self._h, buf, len(shared_ids), shared_tokens, ctypes.byref(out)))
+        return out.value
+
+    def fork(self, seq_id: int) -> int:
+        out = ctypes.c_int32()
+        check(lib().pkv_seq_fork(self._h, seq_id, ctypes.byref(out)))
+        return out.value
+
+    def free_sequence(self, seq_id: int) -> None:
+        check(lib().pkv_seq_free(self._h, seq_id))
+
+    def append_tokens(self, seq_ids: Sequence[int], counts: Optional[Sequence[int]] = None
+                      ) -> Tuple[List[int], List[Tuple[int, int]]]:
+        n = len(seq_ids)
+        ids = (ctypes.c_int32 * max(1, n))(*seq_ids)
+        cnt = None if counts is None else (ctypes.c_int32 * max(1, n))(*counts)
+        total = n if counts is None else sum(int(c) for c in counts)
+        slots = (ctypes.c_int64 * max(1, total))()
+        pairs = (ctypes.c_int64 * max(2, 2 * n))()
+        np_ = ctypes.c_int32()
+        check(lib().pkv_seq_append(self._h, ids, cnt, n, slots, max(0, total), pairs, n, ctypes.byref(np_)))
+        return list(slots[:total]), [(pairs[2 * i], pairs[2 * i + 1]) for i in range(np_.value)]
+
+    def append_tokens_into(self, seq_ids: Sequence[int], slots_out, pairs_out) -> int:
+        """One token per sequence, slots written into a caller buffer (e.g. pinned
+        int64 host memory); returns the number of copy-on-write pairs written."""
+        n = len(seq_ids)
+        ids = (ctypes.c_int32 * max(1, n))(*seq_ids)
+        np_ = ctypes.c_int32()
+        check(lib().pkv_seq_append(self._h, ids, None, n, ctypes.c_void_p(slots_out.data_ptr()), n,
+                                   ctypes.c_void_p(pairs_out.data_ptr()), pairs_out.numel() // 2,
+                                   ctypes.byref(np_)))
+        return np_.value
+
+    def seq_len(self, seq_id: int) -> int:
+        n = ctypes.c_int64()
+        check(lib().pkv_seq_len(self._h, seq_id, ctypes.byref(n)))
+        return n.value
+
+    def block_table(self, seq_id: int) -> List[int]:
+        cap = self.blocks_needed(self.seq_len(seq_id)) + 1
+        buf = (ctypes.c_int32 * cap)()
+        n = ctypes.c_int32()
+        check(lib().pkv_seq_block_table(self._h, seq_id, buf, cap, ctypes.byref(n)))
+        return list(buf[:n.value])
+
+    def fill_tables(self, seq_ids: Sequence[int], max_blocks: int, tables_out: torch.Tensor,
+                    lens_out: torch.Tensor) -> None:
+        """Rows of tables_out [n, max_blocks] int32 and lens_out [n] int32 (CPU tensors)."""
+        if tables_out.device.type != "cpu" or lens_out.device.type != "cpu":
+            raise TypeError("fill_tables writes host tensors")
+        ids = (ctypes.c_int32 * max(1, len(seq_ids)))(*seq_ids)
+        check(lib().pkv_seq_fill_tables(self._h, ids, len(seq_ids), ctypes.c_void_p(tables_out.data_ptr()),
+                                        max_blocks, ctypes.c_void_p(lens_out.data_ptr())))

@@ -1,0 +1,673 @@
+// decode.cu -- a3..a7: fused gather-and-attend decode over the paged pool.
+//
+// What it computes is the plain definition in "How to Implement Paged
+// Attention in PyTorch and vLLM", section "Compute reference attention without
+// hiding the layout": for sequence s and query head h, with KV head
+// h / (Hq / Hkv), softmax over t < L_s of scale * <q, K_t> applied to V_t.
+// "Map the PyTorch design to vLLM PagedAttention" names fused kernels that read
+// the block table during attention instead of gathering; this is one, shaped
+// for GB300:
+//
+//  * Work split (split-K, "flash-decoding"): the 16-token sub-blocks of all
+//    sequences are concatenated and cut into equal contiguous ranges, one per
+//    CTA, one CTA per SM (persistent).  A sequence wholly inside one range is
+//    finished in place; a sequence cut by a range boundary leaves (running max,
+//    running sum, unnormalised output) records in the workspace that
+//    decode_merge_kernel combines.  Balance is exact whatever the length mix.
+//  * Data movement: one producer warp walks the block tables and issues TMA
+//    tensor loads (one 16-token x 64-dim tile, 2 KB, 128-byte swizzle, per KV
+//    head and half of head_dim) into a ring of shared-memory stages guarded by
+//    mbarriers; a stage holds K and V of 16 tokens for every KV head of the CTA.
+//    Each K/V byte is read from HBM once (GQA: the query heads of a group share
+//    it).
+//  * Math: one consumer warp per KV head.  Scores for 16 tokens x the group's
+//    query heads come from mma.sync m16n8k16 (tokens as M, heads as N, fp32
+//    accumulate); the online softmax (running max in base 2, rescaled running
+//    sum and accumulator) follows the online-normaliser recurrence of Milakov &
+//    Gimelshein (2018) as used by FlashAttention-2; P is transposed in
+//    registers (movmatrix) and multiplied with V^T on the tensor cores as a
+//    16-bit hi + lo pair, so P keeps ~16 significant bits.
+#include <cuda.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace pkv {
+
+constexpr int kSub = 16;      // tokens per stage (the mma M dimension)
+constexpr int kTile = 2048;   // bytes of one swizzled 16-token x 64-element tile
+// Consumer warps (one per KV head) per CTA: 8 at head_dim 128 keeps the
+// accumulators in registers (3 warps per SM sub-partition), 16 at head_dim 64.
+template <int D>
+constexpr int max_heads_per_cta() { return D == 64 ? 16 : 8; }
+constexpr int kMinSubBlocksPerCta = 4;
+
+struct DecodeParams {
+    const void *q;
+    int64_t q_stride;              // elements between consecutive query rows
+    const int32_t *tables;
+    int32_t max_blocks;
+    const int32_t *seq_lens;
+    const int32_t *cu_q;           // varlen mode: only q_len == 1 sequences, row cu_q[s]
+    int32_t num_seqs;
+    int32_t num_blocks, block_size, hkv, heads_per_cta, group;
+    float scale_log2;              // scale * log2(e)
+    void *out;
+    int32_t out_f32;
+    float *ws_o;                   // [num_hg][cmax][2][heads_per_cta * group][D]
+    float *ws_ml;                  // [num_hg][cmax][2][heads_per_cta * group][2]
+    int32_t *ws_meta;              // [0] total sub-blocks, [1] CTAs used, [2 + s] first sub-block of s
+    int32_t cmax;                  // gridDim.x
+    int32_t *err;
+    int32_t stages;
+};
+
+// Sub-blocks of sequence s handled by the decode kernel (0 when skipped).
+__device__ __forceinline__ int decode_sub_blocks(const DecodeParams &p, int s) {
+    if (p.cu_q && p.cu_q[s + 1] - p.cu_q[s] != 1) return 0;
+    const int L = p.seq_lens[s];
+    if (L <= 0) return 0;
+    if ((int64_t)L > (int64_t)p.max_blocks * p.block_size) return 0;
+    return (L + kSub - 1) / kSub;
+}
+
+__device__ __forceinline__ bool decode_bad_length(const DecodeParams &p, int s) {
+    if (p.cu_q && p.cu_q[s + 1] - p.cu_q[s] != 1) return false;
+    const int L = p.seq_lens[s];
+    return L < 0 || (int64_t)L > (int64_t)p.max_blocks * p.block_size;
+}
+
+// Inclusive block-wide scan of one int per thread; *total gets the block sum.
+__device__ __forceinline__ int block_scan(int v, int *warp_sums, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < nw) warp_sums[lane] = w;  // inclusive prefix of warp totals
+    }
+    __syncthreads();
+    const int before = warp > 0 ? warp_sums[warp - 1] : 0;
+    *total = warp_sums[nw - 1];
+    __syncthreads();
+    return x + before;
+}
+
+// The CTA that owns concatenated sub-block x when `ctas` ranges split `total`.
+__device__ __forceinline__ int range_owner(int64_t x, int64_t total, int64_t ctas) {
+    return (int)(((x + 1) * ctas - 1) / total);
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
+    decode_splitk_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                         const DecodeParams p) {
+    constexpr int HALVES = D / 64;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int s_warp[32];
+    __shared__ int s_first_seq, s_first_start;
+    __shared__ volatile int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int HG = p.heads_per_cta;
+    const int tiles = HG * HALVES;                 // 2 KB tiles per K (and per V) in a stage
+    const int stage_bytes = 2 * tiles * kTile;
+    const int NS = p.stages;
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + NS * stage_bytes);
+    uint64_t *empty = full + NS;
+    const int hg = blockIdx.y;
+    const bool meta_cta = blockIdx.x == 0 && blockIdx.y == 0;
+
+    // ---- 1. total sub-blocks, this CTA's range ------------------------------
+    int64_t total = 0;
+    for (int s0 = 0; s0 < p.num_seqs; s0 += blockDim.x) {
+        const int s = s0 + tid;
+        const int n = s < p.num_seqs ? decode_sub_blocks(p, s) : 0;
+        if (meta_cta && s < p.num_seqs && decode_bad_length(p, s)) set_err(p.err, PKV_DEVERR_LENGTH);
+        int chunk;
+        block_scan(n, s_warp, &chunk);
+        total += chunk;
+    }
+    const int64_t want = (total + kMinSubBlocksPerCta - 1) / kMinSubBlocksPerCta;
+    const int ctas = (int)(want < gridDim.x ? want : gridDim.x);
+    if (blockIdx.x >= ctas && !meta_cta) return;
+    const int64_t lo = ctas ? (int64_t)blockIdx.x * total / ctas : 0;
+    const int64_t hi = ctas ? (int64_t)(blockIdx.x + 1) * total / ctas : 0;
+
+    if (tid == 0) {
+        s_first_seq = -1;
+        s_abort = 0;
+    }
+    int64_t carry = 0;
+    for (int s0 = 0; s0 < p.num_seqs; s0 += blockDim.x) {
+        const int s = s0 + tid;
+        const int n = s < p.num_seqs ? decode_sub_blocks(p, s) : 0;
+        int chunk;
+        const int incl = block_scan(n, s_warp, &chunk);
+        const int64_t start = carry + incl - n;
+        if (n > 0 && start <= lo && lo < start + n) {
+            s_first_seq = s;
+            s_first_start = (int)start;
+        }
+        if (meta_cta && s < p.num_seqs) p.ws_meta[2 + s] = (int)start;
+        carry += chunk;
+    }
+    if (meta_cta && tid == 0) {
+        p.ws_meta[0] = (int)total;
+        p.ws_meta[1] = ctas;
+        p.ws_meta[2 + p.num_seqs] = (int)total;
+    }
+    if (blockIdx.x >= ctas || lo >= hi) return;
+
+    if (tid == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], HG);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // ---- 2. walk of the range: segments (s, first sub-block, end sub-block) --
+    // Both roles walk the same list; `x` counts concatenated sub-blocks.
+    if (warp == 0) {
+        // ===== producer =====
+        if (lane == 0) {
+            prefetch_tensormap(&tmk);
+            prefetch_tensormap(&tmv);
+        }
+        const uint64_t pol = policy_evict_first();
+        int it = 0;
+        bool aborted = false;
+        int s = s_first_seq;
+        int sb = (int)(lo - s_first_start);
+        int64_t x = lo;
+        while (x < hi && !aborted) {
+            const int n_s = decode_sub_blocks(p, s);
+            if (n_s == 0) {
+                ++s;
+                continue;
+            }
+            const int b1 = (int)(sb + (hi - x) < n_s ? sb + (hi - x) : n_s);
+            const int32_t *trow = p.tables + (int64_t)s * p.max_blocks;
+            for (int j0 = sb; j0 < b1 && !aborted; j0 += 32) {
+                const int jn = min(32, b1 - j0);
+                int row = 0;
+                if (lane < jn) {
+                    const int tok = (j0 + lane) * kSub;
+                    const int lb = tok / p.block_size;
+                    int phys = trow[lb];
+                    if (phys < 0 || phys >= p.num_blocks) {
+                        set_err(p.err, PKV_DEVERR_BLOCK);
+                        phys = 0;
+                    }
+                    row = phys * p.block_size + (tok - lb * p.block_size);
+                }
+                for (int j = 0; j < jn; ++j) {
+                    const int r = __shfl_sync(0xffffffffu, row, j);
+                    const int stage = it % NS;
+                    int okw = 1;
+                    if (lane == 0) okw = mbar_wait(&empty[stage], ((it / NS) & 1) ^ 1, &s_abort);
+                    okw = __shfl_sync(0xffffffffu, okw, 0);
+                    if (!okw) {
+                        aborted = true;
+                        break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(&full[stage], stage_bytes);
+                    __syncwarp();
+                    uint8_t *sbase = base + stage * stage_bytes;
+                    for (int tt = lane; tt < 2 * tiles; tt += 32) {
+                        const int which = tt >= tiles;
+                        const int hh = which ? tt - tiles : tt;
+                        const int head = hg * HG + hh / HALVES;
+                        const int half = hh % HALVES;
+                        tma_load_3d(sbase + tt * kTile, which ? &tmv : &tmk, &full[stage], 0, head * HALVES + half, r,
+                                    pol);
+                    }
+                    ++it;
+                }
+            }
+            x += b1 - sb;
+            ++s;
+            sb = 0;
+        }
+        if (aborted && lane == 0) {
+            s_abort = 1;
+            set_err(p.err, PKV_DEVERR_TIMEOUT);
+        }
+        // drain: the last load issued into each stage must land before the CTA exits
+        if (lane == 0) {
+            const int first = it > NS ? it - NS : 0;
+            for (int k = first; k < it; ++k) {
+                volatile int never = 0;
+                if (!mbar_wait(&full[k % NS], (k / NS) & 1, &never)) set_err(p.err, PKV_DEVERR_TIMEOUT);
+            }
+        }
+        return;
+    }
+    if (warp > HG) return;
+
+    // ===== consumer: KV head kvh =====
+    const int w = warp - 1;
+    const int kvh = hg * HG + w;
+    const int G = p.group;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int hA = 2 * t4, hB = 2 * t4 + 1;
+    const float sl = p.scale_log2;
+    const int qheads_cta = HG * G;
+    int it = 0;
+    bool first_seg = true;
+    int s = s_first_seq;
+    int sb = (int)(lo - s_first_start);
+    int64_t x = lo;
+    while (x < hi) {
+        const int n_s = decode_sub_blocks(p, s);
+        if (n_s == 0) {
+            ++s;
+            continue;
+        }
+        const int b1 = (int)(sb + (hi - x) < n_s ? sb + (hi - x) : n_s);
+        const int L = p.seq_lens[s];
+        const int64_t qrow = p.cu_q ? (int64_t)p.cu_q[s] : (int64_t)s;
+
+        // query fragments: B operand (16 dims x 8 heads), head g of the group
+        uint32_t qf[D / 16][2];
+        {
+            const T *qp = static_cast<const T *>(p.q) + qrow * p.q_stride + (int64_t)(kvh * G + g) * D;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                if (g < G) {
+                    qf[kk][0] = *reinterpret_cast<const uint32_t *>(qp + kk * 16 + 2 * t4);
+                    qf[kk][1] = *reinterpret_cast<const uint32_t *>(qp + kk * 16 + 8 + 2 * t4);
+                } else {
+                    qf[kk][0] = 0u;
+                    qf[kk][1] = 0u;
+                }
+            }
+        }
+        float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+        float o[D / 16][4];
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+        bool aborted = false;
+        for (int j = sb; j < b1; ++j, ++it) {
+            const int stage = it % NS;
+            if (!mbar_wait(&full[stage], (it / NS) & 1, &s_abort)) {
+                aborted = true;
+                break;
+            }
+            const uint8_t *kb = base + stage * stage_bytes + (w * HALVES) * kTile;
+            const uint8_t *vb = kb + tiles * kTile;
+            const int nv = min(kSub, L - j * kSub);
+
+            // S^T[16 tokens x 8 heads] = K q^T
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int chunk = ((kk & 3) << 1) + (lane >> 4);
+                    uint32_t a[4];
+                    ldmatrix_x4(a, smem_u32(kb + (kk >> 2) * kTile + tok * 128 + ((chunk ^ (tok & 7)) << 4)));
+                    mma_16816<T>(sc, a, qf[kk][0], qf[kk][1]);
+                }
+            }
+            float x0 = sc[0] * sl, x1 = sc[1] * sl, x2 = sc[2] * sl, x3 = sc[3] * sl;
+            if (nv < kSub) {
+                if (g >= nv) x0 = x1 = -INFINITY;
+                if (g + 8 >= nv) x2 = x3 = -INFINITY;
+            }
+            if (hA >= G) x0 = x2 = 0.f;
+            if (hB >= G) x1 = x3 = 0.f;
+            float bA = fmaxf(x0, x2), bB = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                bA = fmaxf(bA, __shfl_xor_sync(0xffffffffu, bA, off));
+                bB = fmaxf(bB, __shfl_xor_sync(0xffffffffu, bB, off));
+            }
+            const float nA = fmaxf(mA, bA), nB = fmaxf(mB, bB);
+            const float aA = fast_exp2(mA - nA), aB = fast_exp2(mB - nB);
+            mA = nA;
+            mB = nB;
+            const float p0 = fast_exp2(x0 - nA), p1 = fast_exp2(x1 - nB);
+            const float p2 = fast_exp2(x2 - nA), p3 = fast_exp2(x3 - nB);
+            lA = lA * aA + p0 + p2;
+            lB = lB * aB + p1 + p3;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                o[mt][0] *= aA;
+                o[mt][1] *= aB;
+                o[mt][2] *= aA;
+                o[mt][3] *= aB;
+            }
+            // P as the B operand (16 tokens x 8 heads), hi and lo 16-bit parts
+            const uint32_t h01 = pack2<T>(p0, p1), h23 = pack2<T>(p2, p3);
+            const float2 r01 = unpack2<T>(h01), r23 = unpack2<T>(h23);
+            const uint32_t l01 = pack2<T>(p0 - r01.x, p1 - r01.y), l23 = pack2<T>(p2 - r23.x, p3 - r23.y);
+            const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+            const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+            uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
+            if (nv < kSub) {
+                m01 = (2 * t4 < nv ? 0x0000ffffu : 0u) | (2 * t4 + 1 < nv ? 0xffff0000u : 0u);
+                m23 = (2 * t4 + 8 < nv ? 0x0000ffffu : 0u) | (2 * t4 + 9 < nv ? 0xffff0000u : 0u);
+            }
+            // O^T[16 dims x 8 heads] += V^T P
+            {
+                const int tok = (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    const int cg = mt * 2 + ((lane >> 3) & 1);
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(a, smem_u32(vb + (cg >> 3) * kTile + tok * 128 + (((cg & 7) ^ (tok & 7)) << 4)));
+                    a[0] &= m01;
+                    a[1] &= m01;
+                    a[2] &= m23;
+                    a[3] &= m23;
+                    mma_16816<T>(o[mt], a, bh0, bh1);
+                    mma_16816<T>(o[mt], a, bl0, bl1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+        }
+        if (aborted) {
+            if (lane == 0) {
+                s_abort = 1;
+                set_err(p.err, PKV_DEVERR_TIMEOUT);
+            }
+            return;
+        }
+        // sum over the 8 lanes holding other tokens of the same heads
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            lA += __shfl_xor_sync(0xffffffffu, lA, off);
+            lB += __shfl_xor_sync(0xffffffffu, lB, off);
+        }
+        const bool complete = (sb == 0 && b1 == n_s);
+        if (complete) {
+            const float iA = 1.f / lA, iB = 1.f / lB;
+            const int64_t ob = (qrow * (int64_t)(p.hkv * G) + (int64_t)kvh * G) * D;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const int d0 = mt * 16 + g, d1 = d0 + 8;
+                if (p.out_f32) {
+                    float *op = static_cast<float *>(p.out) + ob;
+                    if (hA < G) {
+                        op[hA * D + d0] = o[mt][0] * iA;
+                        op[hA * D + d1] = o[mt][2] * iA;
+                    }
+                    if (hB < G) {
+                        op[hB * D + d0] = o[mt][1] * iB;
+                        op[hB * D + d1] = o[mt][3] * iB;
+                    }
+                } else {
+                    T *op = static_cast<T *>(p.out) + ob;
+                    if (hA < G) {
+                        op[hA * D + d0] = static_cast<T>(o[mt][0] * iA);
+                        op[hA * D + d1] = static_cast<T>(o[mt][2] * iA);
+                    }
+                    if (hB < G) {
+                        op[hB * D + d0] = static_cast<T>(o[mt][1] * iB);
+                        op[hB * D + d1] = static_cast<T>(o[mt][3] * iB);
+                    }
+                }
+            }
+        } else {
+            const int slot = first_seg ? 0 : 1;
+            const int64_t rec = (((int64_t)hg * p.cmax + blockIdx.x) * 2 + slot) * qheads_cta + (int64_t)w * G;
+            float *wo = p.ws_o + rec * D;
+            float *wml = p.ws_ml + rec * 2;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const int d0 = mt * 16 + g, d1 = d0 + 8;
+                if (hA < G) {
+                    wo[hA * D + d0] = o[mt][0];
+                    wo[hA * D + d1] = o[mt][2];
+                }
+                if (hB < G) {
+                    wo[hB * D + d0] = o[mt][1];
+                    wo[hB * D + d1] = o[mt][3];
+                }
+            }
+            if (g == 0) {
+                if (hA < G) {
+                    wml[hA * 2] = mA;
+                    wml[hA * 2 + 1] = lA;
+                }
+                if (hB < G) {
+                    wml[hB * 2] = mB;
+                    wml[hB * 2 + 1] = lB;
+                }
+            }
+        }
+        first_seg = false;
+        x += b1 - sb;
+        ++s;
+        sb = 0;
+    }
+}
+
+// Combines the records of sequences cut by a range boundary; writes zero rows
+// for empty sequences.  One CTA per sequence.
+template <int D, typename T>
+__global__ void decode_merge_kernel(const DecodeParams p) {
+    const int s = blockIdx.x;
+    if (p.cu_q && p.cu_q[s + 1] - p.cu_q[s] != 1) return;
+    const int64_t qrow = p.cu_q ? (int64_t)p.cu_q[s] : (int64_t)s;
+    const int G = p.group, HG = p.heads_per_cta;
+    const int hq = p.hkv * G;
+    const int64_t total = p.ws_meta[0];
+    const int64_t ctas = p.ws_meta[1];
+    const int64_t start = p.ws_meta[2 + s];
+    const int64_t n = p.ws_meta[3 + s] - start;
+    const int64_t ob = qrow * (int64_t)hq * D;
+    if (n == 0) {
+        for (int i = threadIdx.x; i < hq * D; i += blockDim.x) {
+            if (p.out_f32)
+                static_cast<float *>(p.out)[ob + i] = 0.f;
+            else
+                static_cast<T *>(p.out)[ob + i] = static_cast<T>(0.f);
+        }
+        return;
+    }
+    const int c0 = range_owner(start, total, ctas);
+    const int c1 = range_owner(start + n - 1, total, ctas);
+    if (c0 == c1) return;  // finished by the decode kernel
+    const int64_t lo0 = (int64_t)c0 * total / ctas;
+    const int slot0 = start == lo0 ? 0 : 1;
+    for (int i = threadIdx.x; i < hq * D; i += blockDim.x) {
+        const int h = i / D, d = i - h * D;
+        const int hgi = (h / G) / HG;
+        const int hl = h - hgi * HG * G;
+        float M = -INFINITY;
+        for (int c = c0; c <= c1; ++c) {
+            const int slot = c == c0 ? slot0 : 0;
+            const int64_t rec = (((int64_t)hgi * p.cmax + c) * 2 + slot) * (HG * G) + hl;
+            M = fmaxf(M, p.ws_ml[rec * 2]);
+        }
+        float Lsum = 0.f, acc = 0.f;
+        for (int c = c0; c <= c1; ++c) {
+            const int slot = c == c0 ? slot0 : 0;
+            const int64_t rec = (((int64_t)hgi * p.cmax + c) * 2 + slot) * (HG * G) + hl;
+            const float e = exp2f(p.ws_ml[rec * 2] - M);
+            Lsum += p.ws_ml[rec * 2 + 1] * e;
+            acc += p.ws_o[rec * D + d] * e;
+        }
+        const float v = acc / Lsum;
+        if (p.out_f32)
+            static_cast<float *>(p.out)[ob + i] = v;
+        else
+            static_cast<T *>(p.out)[ob + i] = static_cast<T>(v);
+    }
+}
+
+// ---- host side -------------------------------------------------------------
+
+struct DecodePlan {
+    int heads_per_cta, num_hg, stages, threads, smem_bytes, cmax;
+    size_t meta_bytes, ml_bytes, o_bytes;
+};
+
+static int pick_heads_per_cta(int hkv, int head_dim) {
+    const int halves = head_dim / 64;
+    const int cap = head_dim == 64 ? max_heads_per_cta<64>() : max_heads_per_cta<128>();
+    for (int hg = cap < hkv ? cap : hkv; hg >= 1; --hg)
+        if (hkv % hg == 0 && hg * halves * 2 * kTile <= 64 * 1024) return hg;
+    return 1;
+}
+
+static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static pkv_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, int32_t head_dim, int32_t device,
+                            DecodePlan *pl) {
+    int sms = 0;
+    pkv_status st = sm_count(device, &sms);
+    if (st != PKV_OK) return st;
+    pl->heads_per_cta = pick_heads_per_cta(hkv, head_dim);
+    pl->num_hg = hkv / pl->heads_per_cta;
+    // persistent: all CTAs (one per SM over all head groups) resident at once
+    pl->cmax = sms / pl->num_hg > 0 ? sms / pl->num_hg : 1;
+    const int stage_bytes = pl->heads_per_cta * (head_dim / 64) * 2 * kTile;
+    int ns = (200 * 1024) / stage_bytes;
+    pl->stages = ns > 16 ? 16 : (ns < 2 ? 2 : ns);
+    pl->threads = 32 * (1 + pl->heads_per_cta);
+    pl->smem_bytes = pl->stages * stage_bytes + 1024 + 2 * pl->stages * 8;
+    const int group = num_q_heads / hkv;
+    const size_t recs = (size_t)pl->num_hg * pl->cmax * 2 * pl->heads_per_cta * group;
+    pl->meta_bytes = round256(sizeof(int32_t) * (size_t)(num_seqs + 3));
+    pl->ml_bytes = round256(recs * 2 * sizeof(float));
+    pl->o_bytes = round256(recs * head_dim * sizeof(float));
+    return PKV_OK;
+}
+
+template <int D, typename T>
+static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
+                                  const DecodePlan &pl, cudaStream_t stream) {
+    auto kern = decode_splitk_kernel<D, T>;
+    PKV_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes));
+    dim3 grid(pl.cmax, pl.num_hg);
+    kern<<<grid, pl.threads, pl.smem_bytes, stream>>>(mk, mv, p);
+    PKV_CUDA_TRY(cudaGetLastError());
+    decode_merge_kernel<D, T><<<p.num_seqs, 256, 0, stream>>>(p);
+    PKV_CUDA_TRY(cudaGetLastError());
+    return PKV_OK;
+}
+
+// Shared by pkv_attn_decode (cu_q == NULL) and pkv_attn_varlen (q_len == 1 rows).
+pkv_status run_decode(const void *q, int64_t q_stride, const pkv_cache *cache, const int32_t *tables,
+                      int32_t max_blocks, const int32_t *seq_lens, const int32_t *cu_q, int32_t num_seqs,
+                      int32_t num_q_heads, float scale, void *out, int32_t out_dtype, void *workspace,
+                      size_t workspace_bytes, int32_t *err_word, cudaStream_t stream) {
+    DecodePlan pl;
+    pkv_status st = make_plan(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, -1, &pl);
+    if (st != PKV_OK) return st;
+    const size_t need = pl.meta_bytes + pl.ml_bytes + pl.o_bytes;
+    PKV_CHECK_ARG(workspace && workspace_bytes >= need, PKV_ERR_WORKSPACE,
+                  "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+    PKV_CHECK_ARG((reinterpret_cast<uintptr_t>(workspace) & 255) == 0, PKV_ERR_INVALID_ARG,
+                  "workspace must be 256-byte aligned");
+    CUtensorMap mk, mv;
+    st = encode_pool_map(&mk, cache->k, cache);
+    if (st != PKV_OK) return st;
+    st = encode_pool_map(&mv, cache->v, cache);
+    if (st != PKV_OK) return st;
+    DecodeParams p{};
+    p.q = q;
+    p.q_stride = q_stride;
+    p.tables = tables;
+    p.max_blocks = max_blocks;
+    p.seq_lens = seq_lens;
+    p.cu_q = cu_q;
+    p.num_seqs = num_seqs;
+    p.num_blocks = cache->num_blocks;
+    p.block_size = cache->block_size;
+    p.hkv = cache->num_kv_heads;
+    p.heads_per_cta = pl.heads_per_cta;
+    p.group = num_q_heads / cache->num_kv_heads;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out = out;
+    p.out_f32 = out_dtype == PKV_F32;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    p.ws_meta = reinterpret_cast<int32_t *>(ws);
+    p.ws_ml = reinterpret_cast<float *>(ws + pl.meta_bytes);
+    p.ws_o = reinterpret_cast<float *>(ws + pl.meta_bytes + pl.ml_bytes);
+    p.cmax = pl.cmax;
+    p.err = err_word;
+    p.stages = pl.stages;
+    const bool bf = cache->dtype == PKV_BF16;
+    if (cache->head_dim == 64)
+        return bf ? launch_decode_t<64, __nv_bfloat16>(mk, mv, p, pl, stream)
+                  : launch_decode_t<64, __half>(mk, mv, p, pl, stream);
+    return bf ? launch_decode_t<128, __nv_bfloat16>(mk, mv, p, pl, stream)
+              : launch_decode_t<128, __half>(mk, mv, p, pl, stream);
+}
+
+pkv_status decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, int32_t head_dim,
+                                 int32_t device, size_t *bytes) {
+    DecodePlan pl;
+    pkv_status st = make_plan(num_seqs, num_q_heads, hkv, head_dim, device, &pl);
+    if (st != PKV_OK) return st;
+    *bytes = pl.meta_bytes + pl.ml_bytes + pl.o_bytes;
+    return PKV_OK;
+}
+
+pkv_status check_attention_common(const void *q, int64_t q_stride, const pkv_cache *cache, const int32_t *tables,
+                                  int32_t max_blocks, const int32_t *seq_lens, int32_t num_seqs,
+                                  int32_t num_q_heads, void *out, int32_t out_dtype, const char *what) {
+    pkv_status st = check_cache(cache, what);
+    if (st != PKV_OK) return st;
+    st = check_attention_shapes(cache, num_q_heads);
+    if (st != PKV_OK) return st;
+    PKV_CHECK_ARG(num_seqs >= 0 && max_blocks >= 0, PKV_ERR_INVALID_ARG, "%s: negative size", what);
+    PKV_CHECK_ARG(out_dtype == PKV_F32 || out_dtype == cache->dtype, PKV_ERR_DTYPE,
+                  "%s: out dtype must be F32 or the cache's dtype", what);
+    PKV_CHECK_ARG(q_stride >= (int64_t)num_q_heads * cache->head_dim, PKV_ERR_SHAPE,
+                  "%s: q_token_stride %lld shorter than a row", what, (long long)q_stride);
+    PKV_CHECK_ARG((q_stride % 2) == 0 && (reinterpret_cast<uintptr_t>(q) & 3) == 0, PKV_ERR_INVALID_ARG,
+                  "%s: q rows must be 4-byte aligned", what);
+    if (num_seqs > 0)
+        PKV_CHECK_ARG(q && tables && seq_lens && out, PKV_ERR_INVALID_ARG, "%s: NULL pointer", what);
+    return PKV_OK;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+pkv_status pkv_attn_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t device, size_t *bytes) {
+    PKV_CHECK_ARG(bytes && num_seqs >= 0 && num_kv_heads > 0 && num_q_heads > 0 && head_dim > 0,
+                  PKV_ERR_INVALID_ARG, "bad argument");
+    pkv_status st = decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, device, bytes);
+    return st == PKV_OK ? ok() : st;
+}
+
+pkv_status pkv_attn_decode(const void *q, int64_t q_token_stride, const pkv_cache *cache, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                           float scale, void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                           int32_t *err_word, pkv_stream stream) {
+    pkv_status st = check_attention_common(q, q_token_stride, cache, block_tables, max_blocks_per_seq, seq_lens,
+                                           num_seqs, num_q_heads, out, out_dtype, "pkv_attn_decode");
+    if (st != PKV_OK) return st;
+    if (num_seqs == 0) return ok();
+    st = run_decode(q, q_token_stride, cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
+                    num_q_heads, scale, out, out_dtype, workspace, workspace_bytes, err_word, stream);
+    return st == PKV_OK ? ok() : st;
+}
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+// launch.cpp -- see launch.h.
+#include "launch.h"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace pkv {
+
+pkv_status check_cache(const pkv_cache *c, const char *what) {
+    PKV_CHECK_ARG(c, PKV_ERR_INVALID_ARG, "%s: cache descriptor is NULL", what);
+    PKV_CHECK_ARG(c->k && c->v, PKV_ERR_INVALID_ARG, "%s: cache k/v pointer is NULL", what);
+    PKV_CHECK_ARG(aligned16(c->k) && aligned16(c->v), PKV_ERR_INVALID_ARG,
+                  "%s: cache pointers must be 16-byte aligned", what);
+    PKV_CHECK_ARG(c->dtype == PKV_F16 || c->dtype == PKV_BF16, PKV_ERR_DTYPE,
+                  "%s: cache dtype %d is not F16 or BF16", what, c->dtype);
+    PKV_CHECK_ARG(c->num_blocks > 0 && c->block_size > 0 && c->num_kv_heads > 0 && c->head_dim > 0,
+                  PKV_ERR_SHAPE, "%s: cache geometry must be positive (%d, %d, %d, %d)", what,
+                  c->num_blocks, c->block_size, c->num_kv_heads, c->head_dim);
+    PKV_CHECK_ARG((int64_t)c->num_blocks * c->block_size < (int64_t)1 << 31, PKV_ERR_SHAPE,
+                  "%s: num_blocks * block_size must be < 2^31", what);
+    PKV_CHECK_ARG(((int64_t)c->num_kv_heads * c->head_dim * 2) % 16 == 0, PKV_ERR_UNSUPPORTED,
+                  "%s: a token row (num_kv_heads * head_dim * 2 bytes) must be a multiple of 16", what);
+    return PKV_OK;
+}
+
+pkv_status check_attention_shapes(const pkv_cache *c, int32_t num_q_heads) {
+    PKV_CHECK_ARG(num_q_heads > 0 && num_q_heads % c->num_kv_heads == 0, PKV_ERR_SHAPE,
+                  "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads, c->num_kv_heads);
+    const int group = num_q_heads / c->num_kv_heads;
+    PKV_CHECK_ARG(group == 1 || group == 2 || group == 4 || group == 8, PKV_ERR_UNSUPPORTED,
+                  "query heads per KV head must be 1, 2, 4 or 8 (got %d)", group);
+    PKV_CHECK_ARG(c->head_dim == 64 || c->head_dim == 128, PKV_ERR_UNSUPPORTED,
+                  "head_dim must be 64 or 128 (got %d)", c->head_dim);
+    PKV_CHECK_ARG(c->block_size % 16 == 0 && c->block_size <= 256, PKV_ERR_UNSUPPORTED,
+                  "block_size must be a multiple of 16 up to 256 (got %d)", c->block_size);
+    return PKV_OK;
+}
+
+pkv_status sm_count(int32_t device, int *count) {
+    int dev = device;
+    if (dev < 0) PKV_CUDA_TRY(cudaGetDevice(&dev));
+    PKV_CUDA_TRY(cudaDeviceGetAttribute(count, cudaDevAttrMultiProcessorCount, dev));
+    return PKV_OK;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+pkv_status encode_pool_map(CUtensorMap *map, void *base, const pkv_cache *c) {
+    auto fn = encode_fn();
+    PKV_CHECK_ARG(fn, PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const int tiles = c->num_kv_heads * c->head_dim / 64;
+    cuuint64_t dims[3] = {64, (cuuint64_t)tiles, (cuuint64_t)c->num_blocks * c->block_size};
+    cuuint64_t strides[2] = {128, (cuuint64_t)c->num_kv_heads * c->head_dim * 2};
+    cuuint32_t box[3] = {64, 1, 16};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    PKV_CHECK_ARG(r == CUDA_SUCCESS, PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return PKV_OK;
+}
+
+}  // namespace pkv

@@ -1,0 +1,35 @@
+// launch.h -- host-side helpers shared by the .cu files of libpkv: argument
+// validation, the device's SM count, and TMA tensor-map encoding for the pools.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace pkv {
+
+inline int dtype_bytes(int32_t dt) { return dt == PKV_F32 ? 4 : (dt == PKV_F16 || dt == PKV_BF16) ? 2 : 0; }
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+#define PKV_CUDA_TRY(expr)                                                              \
+    do {                                                                                \
+        cudaError_t e_ = (expr);                                                        \
+        if (e_ != cudaSuccess)                                                          \
+            return pkv::fail(PKV_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_));     \
+    } while (0)
+
+// Checks a pool descriptor: pointers, geometry, type.
+pkv_status check_cache(const pkv_cache *c, const char *what);
+// Shapes compiled for the attention kernels.
+pkv_status check_attention_shapes(const pkv_cache *c, int32_t num_q_heads);
+// SM count of `device` (-1: current device).
+pkv_status sm_count(int32_t device, int *count);
+
+// 3-D tensor map over a pool seen as [rows = num_blocks * block_size]
+// x [num_kv_heads * head_dim / 64 tiles of 64 elements] x [64 elements], box
+// = 16 rows x 1 tile x 64 elements, 128-byte swizzle (a 2 KB shared tile).
+pkv_status encode_pool_map(CUtensorMap *map, void *base, const pkv_cache *c);
+
+}  // namespace pkv

@@ -1,0 +1,176 @@
+"""Decode attention on the GPU against the binary64 oracle (max-abs 2e-3)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import pagedattention_decode_gb300 as P
+import workloads as W
+from tests.cases import TOL, assert_close, decode_case
+
+pytestmark = pytest.mark.gpu
+
+
+def run(case, out_dtype=torch.float32, err=None):
+    c = case.to("cuda")
+    out = P.attn_decode(c.q, c.k_cache, c.v_cache, c.tables, c.lens, c.scale, out_dtype=out_dtype, err=err)
+    torch.cuda.synchronize()
+    return out
+
+
+def test_tiny_workload_exact_lengths():
+    """1 layer, 12/12 heads, D 64, bs 16, fp16, 64-block pool, L = 40/20/16/30."""
+    w = W.tiny_decode()
+    case = decode_case(w.seed, w.lengths, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                       w.dtype, num_blocks=w.num_blocks)
+    assert_close(run(case), case.oracle(), what="tiny")
+
+
+SHAPES = [
+    # hq, hkv, d, bs, dtype
+    (32, 8, 128, 16, "f16"),
+    (32, 8, 128, 32, "bf16"),
+    (12, 12, 64, 16, "f16"),
+    (16, 2, 128, 16, "f16"),   # 8 query heads per KV head
+    (4, 2, 64, 32, "bf16"),    # 2 per KV head
+    (8, 8, 128, 64, "bf16"),
+    (24, 24, 64, 16, "f16"),   # two KV-head groups per sequence
+    (2, 1, 128, 128, "f16"),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,dtype", SHAPES)
+def test_ragged_lengths(hq, hkv, d, bs, dtype):
+    lens = [1, 15, 16, 17, 0, 33, 300, 1000, 127, 2]
+    case = decode_case(11 + hq + bs, lens, hq, hkv, d, bs, dtype, sigma=1.0 if dtype == "f16" else 0.5)
+    got = run(case)
+    assert_close(got, case.oracle(), what=f"{hq}/{hkv}/{d}/{bs}/{dtype}")
+    assert torch.all(got[4] == 0)  # empty sequence -> zero row
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_many_sequences_split_across_ctas(dtype):
+    g = W.generator(5)
+    lens = W.uniform_lengths(g, 300, 1, 700)
+    case = decode_case(6, lens, 32, 8, 128, 16, dtype)
+    assert_close(run(case), case.oracle(), what="300 seqs")
+
+
+def test_one_long_sequence_spans_every_cta():
+    case = decode_case(8, [40000], 8, 2, 128, 16, "bf16", sigma=0.5)
+    assert_close(run(case), case.oracle(), what="40k")
+
+
+def test_skewed_lengths():
+    lens = [1024 << k for k in range(5)] + [3, 5000]
+    case = decode_case(9, lens, 32, 8, 128, 16, "bf16", sigma=0.5)
+    assert_close(run(case), case.oracle(), what="skew")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_16bit_output(dtype):
+    lens = [5, 64, 100, 1000]
+    case = decode_case(10, lens, 32, 8, 128, 16, dtype)
+    got = run(case, out_dtype=W.DTYPES[dtype])
+    assert got.dtype == W.DTYPES[dtype]
+    assert_close(got, case.oracle(), what="16-bit out")
+
+
+def test_block_permutation_gives_identical_bits():
+    """The arithmetic order depends only on logical positions: relocating the
+    physical blocks does not change a single output bit."""
+    lens = [700, 3, 48, 1500]
+    a = decode_case(12, lens, 32, 8, 128, 16, "f16")
+    nb = a.k_cache.shape[0]
+    perm = torch.tensor(W.permutation(W.generator(13), nb))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(nb)
+    k2 = torch.empty_like(a.k_cache)
+    v2 = torch.empty_like(a.v_cache)
+    k2[perm] = a.k_cache
+    v2[perm] = a.v_cache
+    t2 = a.tables.clone()
+    m = t2 >= 0
+    t2[m] = perm[t2[m].long()].int()
+    b = type(a)(a.q, k2, v2, t2, a.lens, a.scale, a.dtype)
+    assert torch.equal(run(a), run(b))
+
+
+def test_block_size_change_within_tolerance():
+    lens = [333, 64, 1]
+    a = decode_case(14, lens, 16, 4, 64, 16, "f16", poison=False)
+    # same logical K/V re-laid out in 32-token blocks
+    g = W.generator(15)
+    tabs, _ = W.scattered_tables(g, lens, 32, 40)
+    k2 = torch.zeros(40, 32, 4, 64, dtype=torch.float16)
+    v2 = torch.zeros_like(k2)
+    for i, L in enumerate(lens):
+        for t in range(L):
+            src = int(a.tables[i, t // 16]), t % 16
+            dst = int(tabs[i, t // 32]), t % 32
+            k2[dst] = a.k_cache[src]
+            v2[dst] = a.v_cache[src]
+    b = type(a)(a.q, k2, v2, tabs, a.lens, a.scale, a.dtype)
+    want = a.oracle()
+    assert np.array_equal(want, b.oracle())
+    assert_close(run(a), want)
+    assert_close(run(b), want)
+
+
+def test_bad_table_entry_is_flagged_not_trapped():
+    case = decode_case(16, [40, 20], 8, 2, 64, 16, "f16")
+    case.tables[1, 0] = case.k_cache.shape[0] + 5
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    run(case, err=err)
+    assert int(err.item()) & P.DEVERR["block"]
+
+
+def test_length_beyond_table_is_flagged():
+    case = decode_case(17, [40, 20], 8, 2, 64, 16, "f16", extra_table_cols=0)
+    case.lens[1] = 10000
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run(case, err=err)
+    assert int(err.item()) & P.DEVERR["length"]
+    assert torch.all(out[1] == 0)
+
+
+def test_gqa_mapping_contiguous_groups():
+    hq, hkv, d, L = 32, 8, 128, 50
+    case = decode_case(18, [L], hq, hkv, d, 16, "f16", poison=False)
+    # V of KV head j is the constant j: output head h must read h // 4
+    case.v_cache[:] = torch.arange(hkv, dtype=torch.float16).view(1, 1, hkv, 1)
+    got = run(case)
+    want = (torch.arange(hq) // (hq // hkv)).float().view(hq, 1).expand(hq, d)
+    assert torch.allclose(got[0].cpu(), want, atol=1e-6)
+
+
+@pytest.mark.parametrize("wl", [W.gqa_decode, W.long_skewed_decode])
+def test_full_size_workload_sampled(wl):
+    """The full-size workloads, launched as the bench launches them; sampled
+    sequences checked against the oracle one by one."""
+    w = wl()
+    dev = "cuda"
+    kc = W.normal_device(w.seed * 10 + 1, (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim), w.sigma,
+                         w.dtype, dev)
+    vc = W.normal_device(w.seed * 10 + 2, kc.shape, w.sigma, w.dtype, dev)
+    g = W.generator(w.seed)
+    q = W.normal(g, (w.batch, w.num_q_heads, w.head_dim), w.sigma, w.dtype)
+    tables, _ = W.scattered_tables(g, w.lengths, w.block_size, w.num_blocks)
+    lens = torch.tensor(w.lengths, dtype=torch.int32)
+    rng = np.random.default_rng(w.seed)
+    picks = sorted(set(rng.choice(w.batch, size=min(6, w.batch), replace=False).tolist()) | {w.batch - 1})
+    # copy the sampled sequences' blocks to the host before any kernel of ours runs
+    samples = []
+    for i in picks:
+        nbk = W.blocks_for(w.lengths[i], w.block_size)
+        ids = tables[i, :nbk].long()
+        samples.append((i, kc[ids.to(dev)].cpu(), vc[ids.to(dev)].cpu()))
+    out = P.attn_decode(q.to(dev), kc, vc, tables.to(dev), lens.to(dev), w.scale)
+    torch.cuda.synchronize()
+    from tests.cases import PagedCase
+    for i, ksub, vsub in samples:
+        nbk = ksub.shape[0]
+        case = PagedCase(q[i:i + 1], ksub, vsub, torch.arange(nbk, dtype=torch.int32).view(1, -1),
+                         lens[i:i + 1], w.scale, w.dtype)
+        assert_close(out[i:i + 1], case.oracle(), what=f"{w.name} seq {i}")

@@ -1,0 +1,66 @@
+"""Packed varlen prefill + decode on the GPU against the binary64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import pagedattention_decode_gb300 as P
+import workloads as W
+from tests.cases import assert_close, varlen_case
+
+pytestmark = pytest.mark.gpu
+
+
+def run(case, causal=True, out_dtype=torch.float32, err=None):
+    c = case.to("cuda")
+    ql = (case.cu_q[1:] - case.cu_q[:-1])
+    out = P.attn_varlen(c.q, c.k_cache, c.v_cache, c.tables, c.cu_q, c.lens, int(ql.max()), c.scale,
+                        causal=causal, out_dtype=out_dtype, err=err)
+    torch.cuda.synchronize()
+    return out
+
+
+SHAPES = [(32, 8, 128, 16, "f16"), (32, 8, 128, 32, "bf16"), (12, 12, 64, 16, "f16"), (16, 2, 128, 16, "bf16"),
+          (4, 2, 64, 32, "f16")]
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,dtype", SHAPES)
+@pytest.mark.parametrize("causal", [True, False])
+def test_mixed_prefill_and_decode(hq, hkv, d, bs, dtype, causal):
+    # chunks of several tiles with ragged tails, a chunk equal to its context,
+    # decode rows, an empty row set and a q_len 2 chunk
+    q_lens = [77, 1, 300, 1, 0, 2, 40, 1]
+    kv_lens = [77 + 200, 50, 300, 1, 5, 2, 40 + 1000, 700]
+    case = varlen_case(31 + hq + bs, q_lens, kv_lens, hq, hkv, d, bs, dtype,
+                       sigma=1.0 if dtype == "f16" else 0.5)
+    assert_close(run(case, causal), case.oracle(causal), what=f"varlen {hq}/{hkv}/{d}/{bs}/{dtype}/{causal}")
+
+
+def test_decode_rows_equal_decode_kernel():
+    """A q_len = 1 row sees every key (page 4's decode-mask bug made it see only the first)."""
+    q_lens = [1, 1, 1]
+    kv_lens = [37, 900, 16]
+    case = varlen_case(41, q_lens, kv_lens, 32, 8, 128, 16)
+    got = run(case)
+    c = case.to("cuda")
+    dec = P.attn_decode(c.q, c.k_cache, c.v_cache, c.tables, c.lens, c.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(got, dec)
+    assert_close(got, case.oracle())
+
+
+def test_square_chunk_is_plain_causal():
+    case = varlen_case(42, [513], [513], 32, 8, 128, 16)
+    assert_close(run(case), case.oracle())
+
+
+def test_16bit_output_varlen():
+    case = varlen_case(43, [129, 1, 64], [1000, 77, 64], 32, 8, 128, 16, "bf16", sigma=0.5)
+    got = run(case, out_dtype=torch.bfloat16)
+    assert_close(got, case.oracle())
+
+
+def test_q_len_beyond_kv_len_is_flagged():
+    case = varlen_case(44, [40, 1], [30, 20], 8, 2, 64, 16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    run(case, err=err)
+    assert int(err.item()) & P.DEVERR["length"]
