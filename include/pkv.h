@@ -162,6 +162,31 @@ PKV_API pkv_status pkv_attn_decode(const void *q, int64_t q_token_stride, const 
                                    float scale, void *out, int32_t out_dtype, void *workspace,
                                    size_t workspace_bytes, int32_t *err_word, pkv_stream stream);
 
+/*
+ * Decode attention without a caller workspace.  The pages have no
+ * counterpart to this call: it exists for callers that cannot allocate device
+ * memory -- a host program embedding libpkv in a process whose device memory
+ * is owned by another runtime's allocator, or a loop that must not call
+ * cudaMalloc because it synchronises the device.  Same arguments, result and
+ * errors as pkv_attn_decode, minus the workspace.
+ *
+ * Its scratch is a fixed array of PKV_NOALLOC_SCRATCH_BYTES inside the
+ * library's device image, present on every device that loads the library
+ * until the process exits.  A call whose split-K records need more (many
+ * sequences or query heads) returns PKV_ERR_WORKSPACE and launches nothing.
+ * The first call on a device looks up the array's address on the current
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  All calls share the one array and nothing needs clearing between
+ * them, but calls that overlap on the GPU (other streams, other threads) race
+ * on it.  The call itself allocates nothing.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+PKV_API pkv_status pkv_attn_decode_noalloc(const void *q, int64_t q_token_stride, const pkv_cache *cache,
+                                           const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                           const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                                           float scale, void *out, int32_t out_dtype, int32_t *err_word,
+                                           pkv_stream stream);
+
 /* ---- a8: packed varlen prefill + decode ---------------------------------- */
 /*
  * [P4] section 02 (the paged FlashAttention-2 kernel reads K/V through the

@@ -58,6 +58,8 @@ SIGNATURES = {
     "pkv_attn_decode_workspace_size": (_i32, [_i32, _i32, _i32, _i32, _i32, _P(_sz)]),
     "pkv_attn_decode": (_i32, [_vp, _i64, _P(PkvCache), _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
                                _vp, _sz, _vp, _vp]),
+    "pkv_attn_decode_noalloc": (_i32, [_vp, _i64, _P(PkvCache), _vp, _i32, _vp, _i32, _i32, _f32, _vp, _i32,
+                                       _vp, _vp]),
     "pkv_attn_varlen_workspace_size": (_i32, [_i32, _i32, _i32, _i32, _i32, _P(_sz)]),
     "pkv_attn_varlen": (_i32, [_vp, _i64, _P(PkvCache), _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
                                _f32, _i32, _vp, _i32, _vp, _sz, _vp, _vp]),
