@@ -396,6 +396,167 @@ def reference_arm(args, rank: int):
 
 
 # ---------------------------------------------------------------------------
+# secondary workload: the mixed packed step with a shared prefix and a beam split
+# ---------------------------------------------------------------------------
+
+class MixedStep:
+    """GQA 32/8, D 128, fp16, block_size 32.  Step 1: a 2048-token prefix
+    shared (whole blocks) by 16 prefill chunks of 512 rows and 240 decode
+    sequences with total contexts U[256, 8192]; 8432 new rows written, then one
+    packed varlen call.  Step 2: 32 decode sequences fork to width 4, each beam
+    appends a token (copy-on-write of non-full shared tails), copy_blocks,
+    write, decode over the 128 beams.  Slots, tables and pairs come from the
+    product allocator, set up once; the timed steps replay them."""
+
+    def __init__(self, dev: torch.device):
+        import pagedattention_decode_gb300 as P
+        self.P, self.dev = P, dev
+        bs, hq, hkv, d, self.dtype = 32, 32, 8, 128, "f16"
+        self.bs, self.hq, self.hkv, self.d = bs, hq, hkv, d
+        self.scale = 1.0 / math.sqrt(d)
+        g = W.generator(5)
+        dec_lens = W.mixed_step_decode_lengths()
+        pre, chunk, nchunk = 2048, 512, 16
+        shared = [min(pre // bs, (L - 1) // bs) for L in dec_lens]
+        need = pre // bs + nchunk * W.blocks_for(pre + chunk, bs)
+        need += sum(W.blocks_for(L, bs) - k for L, k in zip(dec_lens, shared)) + 32 * 4 * 2
+        nb = int(math.ceil(1.1 * need))
+        self.num_blocks = nb
+        al = P.BlockAllocator(nb, bs)
+        al.set_free_order(W.permutation(g, nb))
+        owner = al.create_sequence()
+        al.append_tokens([owner], [pre])
+        prefix = al.block_table(owner)
+        chunks = [al.create_sequence(prefix, pre) for _ in range(nchunk)]
+        decs = []
+        for L, k in zip(dec_lens, shared):
+            sq = al.create_sequence(prefix[:k], k * bs)
+            al.append_tokens([sq], [L - 1 - k * bs])
+            decs.append(sq)
+        seqs = chunks + decs
+        q_lens = [chunk] * nchunk + [1] * len(decs)
+        slots1, pairs = al.append_tokens(seqs, q_lens)
+        assert not pairs
+        self.k_cache = W.normal_device(51, (nb, bs, hkv, d), 1.0, self.dtype, str(dev))
+        self.v_cache = W.normal_device(52, self.k_cache.shape, 1.0, self.dtype, str(dev))
+
+        def tables_of(ids):
+            mb = max(len(al.block_table(x)) for x in ids)
+            t = torch.full((len(ids), mb), -1, dtype=torch.int32)
+            ln = torch.empty(len(ids), dtype=torch.int32)
+            al.fill_tables(ids, mb, t, ln)
+            return t, ln
+
+        t1, l1 = tables_of(seqs)
+        cu = [0]
+        for n in q_lens:
+            cu.append(cu[-1] + n)
+        self.s1 = dict(tables=t1.to(dev), lens=l1.to(dev), cu=torch.tensor(cu, dtype=torch.int32, device=dev),
+                       q=W.normal(g, (cu[-1], hq, d), 1.0, self.dtype).to(dev),
+                       k=W.normal(g, (len(slots1), hkv, d), 1.0, self.dtype).to(dev),
+                       v=W.normal(g, (len(slots1), hkv, d), 1.0, self.dtype).to(dev),
+                       slots=torch.tensor(slots1, dtype=torch.int64, device=dev), max_q=chunk)
+        self.s1_lens_host = l1.tolist()
+        self.q_lens = q_lens
+        # the same rows split by kind, for per-kernel rates
+        tp, lp = tables_of(chunks)
+        self.pf = dict(tables=tp.to(dev), lens=lp.to(dev),
+                       cu=torch.tensor(cu[:nchunk + 1], dtype=torch.int32, device=dev),
+                       q=self.s1["q"][:nchunk * chunk])
+        td, ld = tables_of(decs)
+        self.dc = dict(tables=td.to(dev), lens=ld.to(dev), q=self.s1["q"][nchunk * chunk:])
+        # step 2: beam split of 32 decode sequences
+        pick = sorted(int(x) for x in torch.randperm(len(decs), generator=g)[:32])
+        beams = []
+        for i in pick:
+            beams += [decs[i]] + [al.fork(decs[i]) for _ in range(3)]
+        slots2, pairs2 = al.append_tokens(beams)
+        t2, l2 = tables_of(beams)
+        self.s2 = dict(tables=t2.to(dev), lens=l2.to(dev), q=W.normal(g, (len(beams), hq, d), 1.0, self.dtype).to(dev),
+                       k=W.normal(g, (len(slots2), hkv, d), 1.0, self.dtype).to(dev),
+                       v=W.normal(g, (len(slots2), hkv, d), 1.0, self.dtype).to(dev),
+                       slots=torch.tensor(slots2, dtype=torch.int64, device=dev),
+                       pairs=torch.tensor(pairs2 if pairs2 else [[0, 0]], dtype=torch.int64, device=dev)[:len(pairs2)])
+        self.npairs = len(pairs2)
+        self.s2_lens_host = l2.tolist()
+        self.out1 = torch.empty((cu[-1], hq, d), dtype=torch.float32, device=dev)
+        self.out2 = torch.empty((len(beams), hq, d), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(P.varlen_workspace_size(len(seqs), hq, hkv, d), dtype=torch.uint8, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.pre, self.chunk, self.nchunk, self.ndec = pre, chunk, nchunk, len(decs)
+
+    def step1(self):
+        P, s = self.P, self.s1
+        P.write_kv(s["k"], s["v"], s["slots"], self.k_cache, self.v_cache, err=self.err)
+        P.attn_varlen(s["q"], self.k_cache, self.v_cache, s["tables"], s["cu"], s["lens"], s["max_q"], self.scale,
+                      out=self.out1, workspace=self.ws, err=self.err)
+
+    def step2(self):
+        P, s = self.P, self.s2
+        if self.npairs:
+            P.copy_blocks([self.k_cache], [self.v_cache], s["pairs"], err=self.err)
+        P.write_kv(s["k"], s["v"], s["slots"], self.k_cache, self.v_cache, err=self.err)
+        P.attn_decode(s["q"], self.k_cache, self.v_cache, s["tables"], s["lens"], self.scale, out=self.out2,
+                      workspace=self.ws, err=self.err)
+
+    def prefill_only(self):
+        s = self.pf
+        self.P.attn_varlen(s["q"], self.k_cache, self.v_cache, s["tables"], s["cu"], s["lens"], self.chunk,
+                           self.scale, out=self.out1[:s["q"].shape[0]], workspace=self.ws, err=self.err)
+
+    def decode_only(self):
+        s = self.dc
+        self.P.attn_decode(s["q"], self.k_cache, self.v_cache, s["tables"], s["lens"], self.scale,
+                           out=self.out1[self.nchunk * self.chunk:], workspace=self.ws, err=self.err)
+
+    def prefill_flops(self):
+        # rows i of a chunk see prefix + i + 1 keys; 4 * D flops per key per head
+        keys = sum(self.pre + i + 1 for i in range(self.chunk)) * self.nchunk
+        return 4 * self.d * self.hq * keys
+
+    def decode_rows_bytes(self):
+        lens = self.s1_lens_host[self.nchunk:]
+        sms = torch.cuda.get_device_properties(self.dev).multi_processor_count
+        return decode_bytes(lens, self.hq, self.hkv, self.d, 2, 4, sms)  # logical KV (prefix re-reads included)
+
+
+def time_fn(fn, steps, warmup):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def mixed_main(args):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    m = MixedStep(dev)
+    with ClockSampler(gpu_id_for_smi(dev)) as clk:
+        t1 = time_fn(m.step1, args.steps, args.warmup)
+        t2 = time_fn(m.step2, args.steps, args.warmup)
+        tp = time_fn(m.prefill_only, args.steps, args.warmup)
+        td = time_fn(m.decode_only, args.steps, args.warmup)
+    assert int(m.err.item()) == 0, f"device error word {int(m.err.item())}"
+    fl = m.prefill_flops()
+    db = m.decode_rows_bytes()
+    line = {
+        "workload": "mixed_prefix2048_16x512_prefill_240_decode_bs32_beam4x32", "steps": args.steps,
+        "warmup": args.warmup, "step1_ms": t1, "step2_ms": t2,
+        "step1_rows_per_s": (m.nchunk * m.chunk + m.ndec) / (t1 * 1e-3),
+        "prefill_only_ms": tp, "prefill_tflops": fl / (tp * 1e-3) / 1e12, "prefill_gflop": fl / 1e9,
+        "decode_rows_only_ms": td, "decode_rows_logical_GBps": db / (td * 1e-3) / 1e9,
+        "step2_beams": len(m.s2_lens_host), "step2_cow_pairs": m.npairs, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
 
 def main():
     ap = argparse.ArgumentParser()
@@ -405,6 +566,10 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="gqa", choices=["gqa", "mixed"],
+                    help="gqa: the headline decode step; mixed: the packed prefill+decode step (own line)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="use only the first N sequences (a smaller case of the same workload, for profiling)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -423,6 +588,9 @@ def main():
         if pg is not None:
             pg.barrier()
 
+    if args.workload == "mixed" and args.impl == "pkv":
+        mixed_main(args)
+        return
     if args.impl == "reference":
         reference_arm(args, rank)
         if pg is not None:
@@ -433,6 +601,8 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = W.gqa_decode()
+    if args.batch:
+        w = W.first_sequences(w, args.batch)
     step = DecodeStep(w, dev)
     total_ms, dec_ms, wr_ms, clocks = time_device(step, args.steps, args.warmup, barrier)
     dec_b, wr_b = step.bytes()

@@ -148,7 +148,7 @@ PKV_API pkv_status pkv_write_kv(const void *k, const void *v, int64_t kv_token_s
  *                 ceil(seq_lens[s] / block_size) are never read.
  *   seq_lens      device int32 [num_seqs]; 0 gives an all-zero output row.
  *   scale         multiplies q.k before the softmax (1/sqrt(head_dim) usually).
- *   out           device [num_seqs, num_q_heads, head_dim] of out_dtype
+ *   out           device [num_seqs, num_q_heads, head_dim] of out_dtype, 16-byte aligned
  *                 (PKV_F32, or the cache's dtype).
  *   workspace     device scratch of >= pkv_attn_decode_workspace_size bytes,
  *                 256-byte aligned; its contents on entry do not matter.

@@ -247,6 +247,8 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
             s_abort = 1;
             set_err(p.err, PKV_DEVERR_TIMEOUT);
         }
+        // every load of this CTA is issued: the merge kernel may be scheduled
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         // drain: the last load issued into each stage must land before the CTA exits
         if (lane == 0) {
             const int first = it > NS ? it - NS : 0;
@@ -461,9 +463,16 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
 }
 
 // Combines the records of sequences cut by a range boundary; writes zero rows
-// for empty sequences.  One CTA per sequence.
+// for empty sequences.  One CTA per sequence.  For a cut sequence the CTA
+// first turns the per-part running maxima and sums of every query head into
+// weights exp2(m_c - M) / sum_c(l_c exp2(m_c - M)) in shared memory, then each
+// thread produces 4 consecutive outputs from float4 loads of every part.
+// Launched as a programmatic dependent of the decode kernel: it is scheduled
+// while that kernel drains and waits for its completion before any read.
 template <int D, typename T>
-__global__ void decode_merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
+    extern __shared__ float s_w[];  // [parts][hq] weights of the parts of a cut sequence
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int s = blockIdx.x;
     if (p.cu_q && p.cu_q[s + 1] - p.cu_q[s] != 1) return;
     const int64_t qrow = p.cu_q ? (int64_t)p.cu_q[s] : (int64_t)s;
@@ -486,31 +495,53 @@ __global__ void decode_merge_kernel(const DecodeParams p) {
     const int c0 = range_owner(start, total, ctas);
     const int c1 = range_owner(start + n - 1, total, ctas);
     if (c0 == c1) return;  // finished by the decode kernel
+    const int parts = c1 - c0 + 1;
     const int64_t lo0 = (int64_t)c0 * total / ctas;
     const int slot0 = start == lo0 ? 0 : 1;
-    for (int i = threadIdx.x; i < hq * D; i += blockDim.x) {
-        const int h = i / D, d = i - h * D;
+    auto record = [&](int c, int h) -> int64_t {
         const int hgi = (h / G) / HG;
         const int hl = h - hgi * HG * G;
+        const int slot = c == c0 ? slot0 : 0;
+        return (((int64_t)hgi * p.cmax + c) * 2 + slot) * (HG * G) + hl;
+    };
+    // weights: one warp per query head at a time, lanes over the parts
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    for (int h = warp; h < hq; h += nwarps) {
         float M = -INFINITY;
-        for (int c = c0; c <= c1; ++c) {
-            const int slot = c == c0 ? slot0 : 0;
-            const int64_t rec = (((int64_t)hgi * p.cmax + c) * 2 + slot) * (HG * G) + hl;
-            M = fmaxf(M, p.ws_ml[rec * 2]);
+        for (int c = lane; c < parts; c += 32) M = fmaxf(M, p.ws_ml[record(c0 + c, h) * 2]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float Lsum = 0.f;
+        for (int c = lane; c < parts; c += 32) {
+            const int64_t r = record(c0 + c, h);
+            const float e = exp2f(p.ws_ml[r * 2] - M);
+            s_w[c * hq + h] = e;
+            Lsum += p.ws_ml[r * 2 + 1] * e;
         }
-        float Lsum = 0.f, acc = 0.f;
-        for (int c = c0; c <= c1; ++c) {
-            const int slot = c == c0 ? slot0 : 0;
-            const int64_t rec = (((int64_t)hgi * p.cmax + c) * 2 + slot) * (HG * G) + hl;
-            const float e = exp2f(p.ws_ml[rec * 2] - M);
-            Lsum += p.ws_ml[rec * 2 + 1] * e;
-            acc += p.ws_o[rec * D + d] * e;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
+        const float inv = 1.f / Lsum;
+        for (int c = lane; c < parts; c += 32) s_w[c * hq + h] *= inv;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < hq * (D / 4); i += blockDim.x) {
+        const int h = i / (D / 4), d4 = i - h * (D / 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < parts; ++c) {
+            const float w = s_w[c * hq + h];
+            const float4 o = *reinterpret_cast<const float4 *>(p.ws_o + record(c0 + c, h) * D + 4 * d4);
+            acc.x += w * o.x;
+            acc.y += w * o.y;
+            acc.z += w * o.z;
+            acc.w += w * o.w;
         }
-        const float v = acc / Lsum;
-        if (p.out_f32)
-            static_cast<float *>(p.out)[ob + i] = v;
-        else
-            static_cast<T *>(p.out)[ob + i] = static_cast<T>(v);
+        const int64_t off = ob + (int64_t)h * D + 4 * d4;
+        if (p.out_f32) {
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off) = acc;
+        } else {
+            T *op = static_cast<T *>(p.out) + off;
+            *reinterpret_cast<uint2 *>(op) = make_uint2(pack2<T>(acc.x, acc.y), pack2<T>(acc.z, acc.w));
+        }
     }
 }
 
@@ -561,8 +592,22 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     dim3 grid(pl.cmax, pl.num_hg);
     kern<<<grid, pl.threads, pl.smem_bytes, stream>>>(mk, mv, p);
     PKV_CUDA_TRY(cudaGetLastError());
-    decode_merge_kernel<D, T><<<p.num_seqs, 256, 0, stream>>>(p);
-    PKV_CUDA_TRY(cudaGetLastError());
+    // the merge reads only what the decode kernel wrote: launch it as a
+    // programmatic dependent so it is scheduled while the decode kernel drains
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_seqs);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = (size_t)p.cmax * p.hkv * p.group * sizeof(float);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    auto merge = decode_merge_kernel<D, T>;
+    if (cfg.dynamicSmemBytes > 48 * 1024)
+        PKV_CUDA_TRY(cudaFuncSetAttribute(merge, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes));
+    PKV_CUDA_TRY(cudaLaunchKernelEx(&cfg, merge, p));
     return PKV_OK;
 }
 
@@ -640,6 +685,7 @@ pkv_status check_attention_common(const void *q, int64_t q_stride, const pkv_cac
                   "%s: q rows must be 4-byte aligned", what);
     if (num_seqs > 0)
         PKV_CHECK_ARG(q && tables && seq_lens && out, PKV_ERR_INVALID_ARG, "%s: NULL pointer", what);
+    PKV_CHECK_ARG(aligned16(out), PKV_ERR_INVALID_ARG, "%s: out must be 16-byte aligned", what);
     return PKV_OK;
 }
 

@@ -153,6 +153,14 @@ def long_skewed_decode() -> Workload:
                     lens, int(math.ceil(1.1 * need)), 1.0 / math.sqrt(128))
 
 
+def first_sequences(w: Workload, n: int) -> Workload:
+    """The same workload cut to its first n sequences, pool resized to 1.1x."""
+    lens = list(w.lengths[:n])
+    need = sum(blocks_for(L, w.block_size) for L in lens)
+    return dataclasses.replace(w, name=f"{w.name}_first{n}", lengths=lens,
+                               num_blocks=max(1, int(math.ceil(1.1 * need))))
+
+
 def mixed_step_decode_lengths() -> List[int]:
     """Total contexts of the 240 decode sequences of the mixed step, U[256, 8192]."""
     g = generator(5)
