@@ -195,10 +195,12 @@ PKV_API pkv_status pkv_attn_decode_noalloc(const void *q, int64_t q_token_stride
  * of sequence s, which has q_len = cu_seqlens_q[s+1] - cu_seqlens_q[s] new
  * rows and kv_len = seq_lens[s] keys (the new rows' keys already written),
  * attends keys t <= kv_len - q_len + i when causal != 0, else all kv_len keys.
- * Rows with q_len == 1 take the decode path; longer chunks take a tensor-core
- * tile path.  q_len > kv_len sets PKV_DEVERR_LENGTH and skips the sequence.
+ * Rows with q_len == 1 take the split-K decode path; longer chunks run on the
+ * tcgen05 tensor cores (accumulators in tensor memory).  q_len > kv_len sets
+ * PKV_DEVERR_LENGTH and skips the sequence.
  *
- *   q             device [total_q, num_q_heads, head_dim], row r at r * q_token_stride.
+ *   q             device [total_q, num_q_heads, head_dim], row r at r * q_token_stride;
+ *                 when max_q_len > 1, q and its row stride must be 16-byte aligned.
  *   cu_seqlens_q  device int32 [num_seqs + 1], nondecreasing, cu[0] = 0, cu[num_seqs] = total_q.
  *   max_q_len     host upper bound on any q_len (sizes the tile grid).
  *   out           device [total_q, num_q_heads, head_dim] of out_dtype.

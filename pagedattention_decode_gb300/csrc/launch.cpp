@@ -74,4 +74,19 @@ pkv_status encode_pool_map(CUtensorMap *map, void *base, const pkv_cache *c) {
     return PKV_OK;
 }
 
+pkv_status encode_q_map(CUtensorMap *map, const void *q, int64_t q_stride, int total_q, int hq, int d, int rows,
+                        int dtype) {
+    auto fn = encode_fn();
+    PKV_CHECK_ARG(fn, PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {64, (cuuint64_t)hq * d / 64, (cuuint64_t)total_q};
+    cuuint64_t strides[2] = {128, (cuuint64_t)q_stride * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                    const_cast<void *>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    PKV_CHECK_ARG(r == CUDA_SUCCESS, PKV_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed (%d)", (int)r);
+    return PKV_OK;
+}
+
 }  // namespace pkv

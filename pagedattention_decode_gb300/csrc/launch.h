@@ -32,4 +32,10 @@ pkv_status sm_count(int32_t device, int *count);
 // = 16 rows x 1 tile x 64 elements, 128-byte swizzle (a 2 KB shared tile).
 pkv_status encode_pool_map(CUtensorMap *map, void *base, const pkv_cache *c);
 
+// 3-D tensor map over packed query rows [total_q][Hq * D / 64][64] (row
+// stride q_stride elements), box = `rows` rows x 1 x 64 elements, 128-byte
+// swizzle: one head-half of `rows` consecutive query rows per load.
+pkv_status encode_q_map(CUtensorMap *map, const void *q, int64_t q_stride, int total_q, int hq, int d, int rows,
+                        int dtype);
+
 }  // namespace pkv
