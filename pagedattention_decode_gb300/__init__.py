@@ -11,7 +11,8 @@ Calls (names as in the C ABI, without the ``pkv_`` prefix):
 * :func:`attn_decode` -- one query row per sequence over its paged keys;
 * :func:`attn_varlen` -- packed prefill chunks and decode rows, causal offset;
 * :func:`copy_blocks` -- block copies for copy-on-write;
-* :class:`BlockAllocator` -- host allocator producing tables, slots and pairs.
+* :class:`BlockAllocator` -- host allocator producing tables, slots and pairs;
+* :class:`StepGraph` -- a CUDA graph of a step built from these calls.
 """
 
 from __future__ import annotations
@@ -27,7 +28,7 @@ from ._native import (DEVERR, PKV_BF16, PKV_F16, PKV_F32, DoubleFreeError, Exhau
 __all__ = [
     "write_kv", "attn_decode", "attn_varlen", "copy_blocks", "decode_workspace_size",
     "varlen_workspace_size", "check_copy_pairs", "BlockAllocator", "PkvError", "ExhaustedError",
-    "DoubleFreeError", "DEVERR", "library_path",
+    "DoubleFreeError", "DEVERR", "library_path", "StepGraph",
 ]
 
 _DT = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16, torch.float32: PKV_F32}
@@ -108,12 +109,11 @@ def varlen_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, he
     return n.value
 
 
-def _workspace(nbytes: int, workspace: Optional[torch.Tensor], device) -> torch.Tensor:
+def _workspace(size_fn, workspace: Optional[torch.Tensor], device) -> torch.Tensor:
+    """The caller's workspace as given (the library checks its size), or a new one."""
     if workspace is not None:
-        if workspace.numel() * workspace.element_size() < nbytes:
-            raise ValueError(f"workspace smaller than the {nbytes} bytes needed")
         return workspace
-    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+    return torch.empty(max(size_fn(), 1), dtype=torch.uint8, device=device)
 
 
 def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
@@ -132,7 +132,7 @@ def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
         out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
     elif not out.is_contiguous() or out.shape != q.shape:
         raise ValueError("out must be contiguous [B, Hq, D]")
-    ws = _workspace(decode_workspace_size(B, hq, c.num_kv_heads, d, q.device.index), workspace, q.device)
+    ws = _workspace(lambda: decode_workspace_size(B, hq, c.num_kv_heads, d, q.device.index), workspace, q.device)
     check(lib().pkv_attn_decode(_ptr(q), _row_stride(q, "q"), ctypes.byref(c), _ptr(block_tables),
                                 block_tables.shape[1] if block_tables.dim() == 2 else 0, _ptr(seq_lens), B, hq,
                                 float(scale), _ptr(out), _DT[out.dtype], _ptr(ws),
@@ -159,7 +159,7 @@ def attn_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
         raise ValueError("cu_seqlens_q must have num_seqs + 1 entries")
     if out is None:
         out = torch.empty((total, hq, d), dtype=out_dtype, device=q.device)
-    ws = _workspace(varlen_workspace_size(B, hq, c.num_kv_heads, d, q.device.index), workspace, q.device)
+    ws = _workspace(lambda: varlen_workspace_size(B, hq, c.num_kv_heads, d, q.device.index), workspace, q.device)
     check(lib().pkv_attn_varlen(_ptr(q), _row_stride(q, "q"), ctypes.byref(c), _ptr(block_tables),
                                 block_tables.shape[1], _ptr(cu_seqlens_q), _ptr(seq_lens), B, total,
                                 int(max_q_len), hq, float(scale), 1 if causal else 0, _ptr(out), _DT[out.dtype],
@@ -307,3 +307,34 @@ class BlockAllocator:
         ids = (ctypes.c_int32 * max(1, len(seq_ids)))(*seq_ids)
         check(lib().pkv_seq_fill_tables(self._h, ids, len(seq_ids), ctypes.c_void_p(tables_out.data_ptr()),
                                         max_blocks, ctypes.c_void_p(lens_out.data_ptr())))
+
+
+class StepGraph:
+    """A CUDA graph of one step made of libpkv calls (and any copies between
+    pinned host buffers and the device that surround them).
+
+    Every call of the library is asynchronous on the current stream, allocates
+    nothing and never synchronises the host, so a whole multi-layer step --
+    copy_blocks, write_kv and attn_decode / attn_varlen for every layer -- can
+    be captured once on static buffers and replayed: the per-call host work
+    (argument checks, tensor-map encoding, launches) is paid once at capture.
+    ``fn`` must use the same tensors on every call and pass explicit
+    workspaces; the first call of pkv_attn_decode_noalloc on a device must
+    come before the capture.
+    """
+
+    def __init__(self, fn, warmup: int = 2):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            fn()
+        torch.cuda.synchronize()
+
+    def replay(self) -> None:
+        self.graph.replay()

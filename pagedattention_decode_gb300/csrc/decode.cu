@@ -466,11 +466,12 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
 // for empty sequences.  One CTA per sequence.  For a cut sequence the CTA
 // first turns the per-part running maxima and sums of every query head into
 // weights exp2(m_c - M) / sum_c(l_c exp2(m_c - M)) in shared memory, then each
-// thread produces 4 consecutive outputs from float4 loads of every part.
+// thread produces 4 consecutive outputs from float4 loads of every part, eight
+// parts in flight at a time (a 128k-token sequence is cut into ~76 parts).
 // Launched as a programmatic dependent of the decode kernel: it is scheduled
 // while that kernel drains and waits for its completion before any read.
 template <int D, typename T>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(512) decode_merge_kernel(const DecodeParams p) {
     extern __shared__ float s_w[];  // [parts][hq] weights of the parts of a cut sequence
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int s = blockIdx.x;
@@ -526,21 +527,46 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
     __syncthreads();
     for (int i = threadIdx.x; i < hq * (D / 4); i += blockDim.x) {
         const int h = i / (D / 4), d4 = i - h * (D / 4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < parts; ++c) {
-            const float w = s_w[c * hq + h];
-            const float4 o = *reinterpret_cast<const float4 *>(p.ws_o + record(c0 + c, h) * D + 4 * d4);
-            acc.x += w * o.x;
-            acc.y += w * o.y;
-            acc.z += w * o.z;
-            acc.w += w * o.w;
+        // independent partial sums so the loads of several parts are in flight at once
+        float4 acc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        int c = 0;
+        for (; c + 8 <= parts; c += 8) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float w = s_w[(c + u) * hq + h];
+                const float4 o = *reinterpret_cast<const float4 *>(p.ws_o + record(c0 + c + u, h) * D + 4 * d4);
+                acc[u].x += w * o.x;
+                acc[u].y += w * o.y;
+                acc[u].z += w * o.z;
+                acc[u].w += w * o.w;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 7; ++u) {
+            if (c + u < parts) {
+                const float w = s_w[(c + u) * hq + h];
+                const float4 o = *reinterpret_cast<const float4 *>(p.ws_o + record(c0 + c + u, h) * D + 4 * d4);
+                acc[u].x += w * o.x;
+                acc[u].y += w * o.y;
+                acc[u].z += w * o.z;
+                acc[u].w += w * o.w;
+            }
+        }
+#pragma unroll
+        for (int u = 1; u < 8; ++u) {
+            acc[0].x += acc[u].x;
+            acc[0].y += acc[u].y;
+            acc[0].z += acc[u].z;
+            acc[0].w += acc[u].w;
         }
         const int64_t off = ob + (int64_t)h * D + 4 * d4;
         if (p.out_f32) {
-            *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off) = acc;
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off) = acc[0];
         } else {
             T *op = static_cast<T *>(p.out) + off;
-            *reinterpret_cast<uint2 *>(op) = make_uint2(pack2<T>(acc.x, acc.y), pack2<T>(acc.z, acc.w));
+            *reinterpret_cast<uint2 *>(op) = make_uint2(pack2<T>(acc[0].x, acc[0].y), pack2<T>(acc[0].z, acc[0].w));
         }
     }
 }
@@ -575,7 +601,7 @@ static pkv_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, 
     int ns = (200 * 1024) / stage_bytes;
     pl->stages = ns > 16 ? 16 : (ns < 2 ? 2 : ns);
     pl->threads = 32 * (1 + pl->heads_per_cta);
-    pl->smem_bytes = pl->stages * stage_bytes + 1024 + 2 * pl->stages * 8;
+    pl->smem_bytes = pl->stages * stage_bytes + 1024 + 2 * pl->stages * 8;  // <= 210 KB (set once per device)
     const int group = num_q_heads / hkv;
     const size_t recs = (size_t)pl->num_hg * pl->cmax * 2 * pl->heads_per_cta * group;
     pl->meta_bytes = round256(sizeof(int32_t) * (size_t)(num_seqs + 3));
@@ -588,7 +614,10 @@ template <int D, typename T>
 static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
                                   const DecodePlan &pl, cudaStream_t stream) {
     auto kern = decode_splitk_kernel<D, T>;
-    PKV_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes));
+    // the plan's shared memory depends only on (D, heads per CTA); size for the largest plan once
+    static std::atomic<uint64_t> smem_set{0};
+    pkv_status st = set_smem_once(reinterpret_cast<const void *>(kern), 210 * 1024, &smem_set);
+    if (st != PKV_OK) return st;
     dim3 grid(pl.cmax, pl.num_hg);
     kern<<<grid, pl.threads, pl.smem_bytes, stream>>>(mk, mv, p);
     PKV_CUDA_TRY(cudaGetLastError());
@@ -596,7 +625,7 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     // programmatic dependent so it is scheduled while the decode kernel drains
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.num_seqs);
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(512);
     cfg.dynamicSmemBytes = (size_t)p.cmax * p.hkv * p.group * sizeof(float);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -605,8 +634,11 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     auto merge = decode_merge_kernel<D, T>;
-    if (cfg.dynamicSmemBytes > 48 * 1024)
-        PKV_CUDA_TRY(cudaFuncSetAttribute(merge, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes));
+    if (cfg.dynamicSmemBytes > 48 * 1024) {
+        static std::atomic<uint64_t> merge_smem_set{0};
+        st = set_smem_once(reinterpret_cast<const void *>(merge), 200 * 1024, &merge_smem_set);
+        if (st != PKV_OK) return st;
+    }
     PKV_CUDA_TRY(cudaLaunchKernelEx(&cfg, merge, p));
     return PKV_OK;
 }

@@ -3,6 +3,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 namespace pkv {
@@ -38,9 +39,25 @@ pkv_status check_attention_shapes(const pkv_cache *c, int32_t num_q_heads) {
 }
 
 pkv_status sm_count(int32_t device, int *count) {
+    static std::atomic<int> cached[64] = {};
     int dev = device;
     if (dev < 0) PKV_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev >= 0 && dev < 64 && cached[dev].load(std::memory_order_relaxed) > 0) {
+        *count = cached[dev].load(std::memory_order_relaxed);
+        return PKV_OK;
+    }
     PKV_CUDA_TRY(cudaDeviceGetAttribute(count, cudaDevAttrMultiProcessorCount, dev));
+    if (dev >= 0 && dev < 64) cached[dev].store(*count, std::memory_order_relaxed);
+    return PKV_OK;
+}
+
+pkv_status set_smem_once(const void *kernel, int bytes, std::atomic<uint64_t> *done) {
+    int dev = 0;
+    PKV_CUDA_TRY(cudaGetDevice(&dev));
+    const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+    if (bit && (done->load(std::memory_order_acquire) & bit)) return PKV_OK;
+    PKV_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+    if (bit) done->fetch_or(bit, std::memory_order_acq_rel);
     return PKV_OK;
 }
 

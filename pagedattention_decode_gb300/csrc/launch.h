@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "internal.h"
 
 namespace pkv {
@@ -24,8 +26,12 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 pkv_status check_cache(const pkv_cache *c, const char *what);
 // Shapes compiled for the attention kernels.
 pkv_status check_attention_shapes(const pkv_cache *c, int32_t num_q_heads);
-// SM count of `device` (-1: current device).
+// SM count of `device` (-1: current device), cached per device.
 pkv_status sm_count(int32_t device, int *count);
+
+// Sets a kernel's max dynamic shared memory once per device (the attribute
+// persists for the process); `done` is that kernel's per-device flag set.
+pkv_status set_smem_once(const void *kernel, int bytes, std::atomic<uint64_t> *done);
 
 // 3-D tensor map over a pool seen as [rows = num_blocks * block_size]
 // x [num_kv_heads * head_dim / 64 tiles of 64 elements] x [64 elements], box

@@ -440,7 +440,9 @@ static pkv_status launch_prefill_tc_t(const CUtensorMap &mq, const CUtensorMap &
     // + 1 KB for the 1024-byte alignment of the swizzled tiles, + 4 KB of slack after the last stage
     const int smem = HALVES * 128 * 128 + kStages * 2 * HALVES * kTok * 128 + 1024 + 4096;
     auto kern = prefill_tc_kernel<D, T>;
-    PKV_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    static std::atomic<uint64_t> smem_set{0};
+    pkv_status st = set_smem_once(reinterpret_cast<const void *>(kern), smem, &smem_set);
+    if (st != PKV_OK) return st;
     dim3 grid(p.q_tiles, num_seqs, p.hkv);
     kern<<<grid, 192, smem, stream>>>(mq, mk, mv, p);
     PKV_CUDA_TRY(cudaGetLastError());
