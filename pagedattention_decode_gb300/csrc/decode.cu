@@ -463,29 +463,34 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
 }
 
 // Combines the records of sequences cut by a range boundary; writes zero rows
-// for empty sequences.  One CTA per sequence.  For a cut sequence the CTA
-// first turns the per-part running maxima and sums of every query head into
-// weights exp2(m_c - M) / sum_c(l_c exp2(m_c - M)) in shared memory, then each
-// thread produces 4 consecutive outputs from float4 loads of every part, eight
-// parts in flight at a time (a 128k-token sequence is cut into ~76 parts).
+// for empty sequences.  Grid: (sequence, group of kMergeHeads query heads).
+// For a cut sequence the CTA first turns the per-part running maxima and sums
+// of its heads into weights exp2(m_c - M) / sum_c(l_c exp2(m_c - M)) in shared
+// memory; then its threads split the parts between them (a 128k-token
+// sequence is cut into ~76 parts), each summing float4 outputs of its parts
+// with four loads in flight, and the part-groups are added in shared memory.
 // Launched as a programmatic dependent of the decode kernel: it is scheduled
 // while that kernel drains and waits for its completion before any read.
-template <int D, typename T>
-__global__ void __launch_bounds__(512) decode_merge_kernel(const DecodeParams p) {
-    extern __shared__ float s_w[];  // [parts][hq] weights of the parts of a cut sequence
+constexpr int kMergeThreads = 512;
+
+template <int D, typename T, int kMergeHeads>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
+    extern __shared__ float4 s_merge[];  // [groups][kMergeHeads * D / 4] partial sums, then [parts][heads] weights
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int s = blockIdx.x;
     if (p.cu_q && p.cu_q[s + 1] - p.cu_q[s] != 1) return;
     const int64_t qrow = p.cu_q ? (int64_t)p.cu_q[s] : (int64_t)s;
     const int G = p.group, HG = p.heads_per_cta;
     const int hq = p.hkv * G;
+    const int h0 = blockIdx.y * kMergeHeads;
+    const int nh = min(kMergeHeads, hq - h0);
     const int64_t total = p.ws_meta[0];
     const int64_t ctas = p.ws_meta[1];
     const int64_t start = p.ws_meta[2 + s];
     const int64_t n = p.ws_meta[3 + s] - start;
-    const int64_t ob = qrow * (int64_t)hq * D;
+    const int64_t ob = (qrow * (int64_t)hq + h0) * D;
     if (n == 0) {
-        for (int i = threadIdx.x; i < hq * D; i += blockDim.x) {
+        for (int i = threadIdx.x; i < nh * D; i += blockDim.x) {
             if (p.out_f32)
                 static_cast<float *>(p.out)[ob + i] = 0.f;
             else
@@ -505,9 +510,13 @@ __global__ void __launch_bounds__(512) decode_merge_kernel(const DecodeParams p)
         const int slot = c == c0 ? slot0 : 0;
         return (((int64_t)hgi * p.cmax + c) * 2 + slot) * (HG * G) + hl;
     };
-    // weights: one warp per query head at a time, lanes over the parts
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-    for (int h = warp; h < hq; h += nwarps) {
+    constexpr int OUTS = kMergeHeads * D / 4;          // float4 outputs of a full head group
+    constexpr int GROUPS = kMergeThreads / OUTS;        // part groups
+    float *s_w = reinterpret_cast<float *>(s_merge + GROUPS * OUTS);
+    // weights: one warp per head, lanes over the parts
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < nh) {
+        const int h = h0 + warp;
         float M = -INFINITY;
         for (int c = lane; c < parts; c += 32) M = fmaxf(M, p.ws_ml[record(c0 + c, h) * 2]);
 #pragma unroll
@@ -516,57 +525,67 @@ __global__ void __launch_bounds__(512) decode_merge_kernel(const DecodeParams p)
         for (int c = lane; c < parts; c += 32) {
             const int64_t r = record(c0 + c, h);
             const float e = exp2f(p.ws_ml[r * 2] - M);
-            s_w[c * hq + h] = e;
+            s_w[c * kMergeHeads + warp] = e;
             Lsum += p.ws_ml[r * 2 + 1] * e;
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
         const float inv = 1.f / Lsum;
-        for (int c = lane; c < parts; c += 32) s_w[c * hq + h] *= inv;
+        for (int c = lane; c < parts; c += 32) s_w[c * kMergeHeads + warp] *= inv;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < hq * (D / 4); i += blockDim.x) {
-        const int h = i / (D / 4), d4 = i - h * (D / 4);
-        // independent partial sums so the loads of several parts are in flight at once
-        float4 acc[8];
+    // partial sums: thread = (part group, output)
+    const int o = threadIdx.x % OUTS, grp = threadIdx.x / OUTS;
+    const int hl = o / (D / 4), d4 = o - hl * (D / 4);
+    float4 acc[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        int c = 0;
-        for (; c + 8 <= parts; c += 8) {
+    for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (hl < nh) {
+        const int h = h0 + hl;
+        int c = grp;
+        for (; c + 3 * GROUPS < parts; c += 4 * GROUPS) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float w = s_w[(c + u) * hq + h];
-                const float4 o = *reinterpret_cast<const float4 *>(p.ws_o + record(c0 + c + u, h) * D + 4 * d4);
-                acc[u].x += w * o.x;
-                acc[u].y += w * o.y;
-                acc[u].z += w * o.z;
-                acc[u].w += w * o.w;
+            for (int u = 0; u < 4; ++u) {
+                const int cc = c + u * GROUPS;
+                const float w = s_w[cc * kMergeHeads + hl];
+                const float4 v = *reinterpret_cast<const float4 *>(p.ws_o + record(c0 + cc, h) * D + 4 * d4);
+                acc[u].x += w * v.x;
+                acc[u].y += w * v.y;
+                acc[u].z += w * v.z;
+                acc[u].w += w * v.w;
             }
         }
 #pragma unroll
-        for (int u = 0; u < 7; ++u) {
-            if (c + u < parts) {
-                const float w = s_w[(c + u) * hq + h];
-                const float4 o = *reinterpret_cast<const float4 *>(p.ws_o + record(c0 + c + u, h) * D + 4 * d4);
-                acc[u].x += w * o.x;
-                acc[u].y += w * o.y;
-                acc[u].z += w * o.z;
-                acc[u].w += w * o.w;
+        for (int u = 0; u < 3; ++u) {
+            const int cc = c + u * GROUPS;
+            if (cc < parts) {
+                const float w = s_w[cc * kMergeHeads + hl];
+                const float4 v = *reinterpret_cast<const float4 *>(p.ws_o + record(c0 + cc, h) * D + 4 * d4);
+                acc[u].x += w * v.x;
+                acc[u].y += w * v.y;
+                acc[u].z += w * v.z;
+                acc[u].w += w * v.w;
             }
         }
-#pragma unroll
-        for (int u = 1; u < 8; ++u) {
-            acc[0].x += acc[u].x;
-            acc[0].y += acc[u].y;
-            acc[0].z += acc[u].z;
-            acc[0].w += acc[u].w;
+    }
+    s_merge[grp * OUTS + o] = make_float4(acc[0].x + acc[1].x + acc[2].x + acc[3].x, acc[0].y + acc[1].y + acc[2].y + acc[3].y,
+                                          acc[0].z + acc[1].z + acc[2].z + acc[3].z, acc[0].w + acc[1].w + acc[2].w + acc[3].w);
+    __syncthreads();
+    if (grp == 0 && hl < nh) {
+        float4 r = s_merge[o];
+        for (int g2 = 1; g2 < GROUPS; ++g2) {
+            const float4 t = s_merge[g2 * OUTS + o];
+            r.x += t.x;
+            r.y += t.y;
+            r.z += t.z;
+            r.w += t.w;
         }
-        const int64_t off = ob + (int64_t)h * D + 4 * d4;
+        const int64_t off = ob + (int64_t)hl * D + 4 * d4;
         if (p.out_f32) {
-            *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off) = acc[0];
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off) = r;
         } else {
             T *op = static_cast<T *>(p.out) + off;
-            *reinterpret_cast<uint2 *>(op) = make_uint2(pack2<T>(acc[0].x, acc[0].y), pack2<T>(acc[0].z, acc[0].w));
+            *reinterpret_cast<uint2 *>(op) = make_uint2(pack2<T>(r.x, r.y), pack2<T>(r.z, r.w));
         }
     }
 }
@@ -623,22 +642,22 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     PKV_CUDA_TRY(cudaGetLastError());
     // the merge reads only what the decode kernel wrote: launch it as a
     // programmatic dependent so it is scheduled while the decode kernel drains
+    // few sequences: 4 query heads per merge CTA (more CTAs share a long
+    // sequence's parts); many sequences: 8 (fewer, mostly idle, CTAs)
+    const bool wide = p.num_seqs >= 128;
+    const int mh = wide ? 8 : 4;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.num_seqs);
-    cfg.blockDim = dim3(512);
-    cfg.dynamicSmemBytes = (size_t)p.cmax * p.hkv * p.group * sizeof(float);
+    const int hq = p.hkv * p.group;
+    cfg.gridDim = dim3(p.num_seqs, (hq + mh - 1) / mh);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = (size_t)kMergeThreads * sizeof(float4) + (size_t)p.cmax * mh * sizeof(float);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    auto merge = decode_merge_kernel<D, T>;
-    if (cfg.dynamicSmemBytes > 48 * 1024) {
-        static std::atomic<uint64_t> merge_smem_set{0};
-        st = set_smem_once(reinterpret_cast<const void *>(merge), 200 * 1024, &merge_smem_set);
-        if (st != PKV_OK) return st;
-    }
+    auto merge = wide ? decode_merge_kernel<D, T, 8> : decode_merge_kernel<D, T, 4>;
     PKV_CUDA_TRY(cudaLaunchKernelEx(&cfg, merge, p));
     return PKV_OK;
 }

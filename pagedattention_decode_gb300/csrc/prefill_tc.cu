@@ -321,13 +321,28 @@ __global__ void __launch_bounds__(192, 2)
             tmem_ld32(trow_addr + b * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
             tmem_wait_ld();
             const int t0 = j * kTok;
-            float mx = -INFINITY;
+            // eight independent partial maxima (short dependency chains);
+            // tiles every row of the warp sees in full skip the causal select
+            float pm[8];
 #pragma unroll
-            for (int c = 0; c < kTok; ++c) {
-                const float x = (t0 + c <= lim) ? __uint_as_float(sr[c]) * sl : -INFINITY;
-                sr[c] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
+            for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
+            if (__all_sync(0xffffffffu, t0 + kTok - 1 <= lim)) {
+#pragma unroll
+                for (int c = 0; c < kTok; ++c) {
+                    const float x = __uint_as_float(sr[c]) * sl;
+                    sr[c] = __float_as_uint(x);
+                    pm[c & 7] = fmaxf(pm[c & 7], x);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kTok; ++c) {
+                    const float x = (t0 + c <= lim) ? __uint_as_float(sr[c]) * sl : -INFINITY;
+                    sr[c] = __float_as_uint(x);
+                    pm[c & 7] = fmaxf(pm[c & 7], x);
+                }
             }
+            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
             const float m_new = fmaxf(m_used, mx);
             const bool need = m_new > m_used + kRescaleLog2;
             const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
@@ -354,16 +369,20 @@ __global__ void __launch_bounds__(192, 2)
                 m_used = m_new;
             }
             uint32_t ph[32], pl[32];
+            float ps[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) ps[u] = 0.f;
 #pragma unroll
             for (int c = 0; c < kTok; c += 2) {
                 const float p0 = fast_exp2(__uint_as_float(sr[c]) - m_used);
                 const float p1 = fast_exp2(__uint_as_float(sr[c + 1]) - m_used);
-                lsum += p0 + p1;
+                ps[(c >> 1) & 7] += p0 + p1;
                 const uint32_t h = pack2<T>(p0, p1);
                 const float2 hf = unpack2<T>(h);
                 ph[c / 2] = h;
                 pl[c / 2] = pack2<T>(p0 - hf.x, p1 - hf.y);
             }
+            lsum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             tmem_st32(trow_addr + b * 64, ph);
             tmem_st32(trow_addr + b * 64 + 32, pl);
             // V rows past kv_len in this tile hold stale or unrelated data: zero them
