@@ -67,7 +67,7 @@ def lib():
         L.oracle_paged_attention.restype = i32
         L.oracle_paged_attention.argtypes = [vp, i64, vp, vp, i32, i64, i32, i32, i32,
                                              vp, i32, vp, vp, i32, i32,
-                                             ctypes.c_double, i32, vp]
+                                             ctypes.c_double, i32, i32, vp]
         _lib = L
     return _lib
 
@@ -100,12 +100,13 @@ def dtype_code(name) -> int:
 
 
 def paged_attention(q, k_cache, v_cache, dtype, block_tables, kv_lens, scale: float,
-                    cu_q: Optional[np.ndarray] = None, causal: bool = False) -> np.ndarray:
+                    cu_q: Optional[np.ndarray] = None, causal: bool = False, window: int = 0) -> np.ndarray:
     """binary64 paged attention.
 
     q: [rows, Hq, D]; caches: [num_blocks, block_size, Hkv, D] (16-bit floats
     of ``dtype``); block_tables [B, max_blocks] int32; kv_lens [B] int32;
-    cu_q [B+1] int32 or None (one row per sequence).  Returns [rows, Hq, D].
+    cu_q [B+1] int32 or None (one row per sequence); window > 0 keeps only the
+    most recent ``window`` keys of each row.  Returns [rows, Hq, D].
     """
     qb, kb, vb = _bits(q), _bits(k_cache), _bits(v_cache)
     nb, bs, hkv, d = kb.shape
@@ -119,7 +120,7 @@ def paged_attention(q, k_cache, v_cache, dtype, block_tables, kv_lens, scale: fl
     rc = lib().oracle_paged_attention(_ptr(qb), hq * d, _ptr(kb), _ptr(vb), dtype_code(dtype),
                                       nb, bs, hkv, d, _ptr(tables), tables.shape[1], _ptr(lens),
                                       None if cu is None else _ptr(cu), B, hq,
-                                      float(scale), 1 if causal else 0, _ptr(out))
+                                      float(scale), 1 if causal else 0, int(window), _ptr(out))
     if rc != 0:
         raise ValueError("oracle_paged_attention rejected its inputs")
     return out

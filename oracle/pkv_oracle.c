@@ -137,6 +137,11 @@ int oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, int64_t num_blocks,
  *   cu_q     [num_seqs + 1]: sequence s owns query rows cu_q[s] .. cu_q[s+1]-1;
  *            NULL means one query row per sequence (decode).
  *   causal   0: every row sees all kv_len keys; 1: row i sees t <= kv_len - q_len + i.
+ *   window   > 0: a row whose last visible key is `last` sees only keys
+ *            t >= last - window + 1 (the most recent `window` tokens, its own
+ *            included; "How to Implement Paged Attention in PyTorch and vLLM",
+ *            section "PagedAttention vs sliding-window attention..."); <= 0: no
+ *            window.
  *   out      [total_rows, num_q_heads, head_dim] binary64.
  *
  * A row that sees no key (kv_len == 0) is all zeros.  Returns 0, or -1 on an
@@ -149,7 +154,7 @@ int oracle_paged_attention(const uint16_t *q, int64_t q_row_stride,
                            int64_t num_blocks, int block_size, int num_kv_heads, int head_dim,
                            const int32_t *tables, int max_blocks, const int32_t *kv_lens,
                            const int32_t *cu_q, int num_seqs, int num_q_heads,
-                           double scale, int causal, double *out)
+                           double scale, int causal, int window, double *out)
 {
     if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
         return -1;
@@ -202,9 +207,12 @@ int oracle_paged_attention(const uint16_t *q, int64_t q_row_stride,
 
             for (int64_t i = 0; i < qlen; ++i) {
                 const int64_t row = row0 + i;
-                int64_t visible = L; /* keys 0 .. visible-1 */
+                int64_t visible = L; /* keys first .. visible-1 */
                 if (causal)
                     visible = L - qlen + i + 1;
+                int64_t first = 0;
+                if (window > 0 && visible - window > 0)
+                    first = visible - window;
                 for (int h = g * group; h < (g + 1) * group; ++h) {
                     double *o = out + (row * num_q_heads + h) * (int64_t)D;
                     for (int d = 0; d < D; ++d)
@@ -214,7 +222,7 @@ int oracle_paged_attention(const uint16_t *q, int64_t q_row_stride,
                     for (int d = 0; d < D; ++d)
                         qd[d] = decode(q[row * q_row_stride + (int64_t)h * D + d], dtype);
                     double mx = -INFINITY;
-                    for (int64_t t = 0; t < visible; ++t) {
+                    for (int64_t t = first; t < visible; ++t) {
                         double dot = 0.0;
                         for (int d = 0; d < D; ++d)
                             dot += qd[d] * K[t * D + d];
@@ -223,11 +231,11 @@ int oracle_paged_attention(const uint16_t *q, int64_t q_row_stride,
                             mx = p[t];
                     }
                     double Z = 0.0;
-                    for (int64_t t = 0; t < visible; ++t) {
+                    for (int64_t t = first; t < visible; ++t) {
                         p[t] = exp(p[t] - mx);
                         Z += p[t];
                     }
-                    for (int64_t t = 0; t < visible; ++t)
+                    for (int64_t t = first; t < visible; ++t)
                         for (int d = 0; d < D; ++d)
                             o[d] += p[t] * V[t * D + d];
                     for (int d = 0; d < D; ++d)

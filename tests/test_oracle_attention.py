@@ -227,3 +227,33 @@ def test_rejects_bad_table_entry():
     bad[0, 1] = 99
     with pytest.raises(ValueError):
         oracle.paged_attention(q, kc, vc, "f16", bad, [20], 0.5)
+
+
+def test_window_pins():
+    """Sliding window ('How to Implement Paged Attention in PyTorch and vLLM',
+    section 'PagedAttention vs sliding-window attention...'): a row attends only
+    to the most recent w tokens, its own included."""
+    lens = [45, 64, 7]
+    bs = 16
+    q, ks, vs, kc, vc, tables = rand_case(40, lens, 4, 2, 16, bs, 16)
+    full = oracle.paged_attention(q, kc, vc, "f16", tables, lens, 0.3)
+    # a window at least as long as the context changes nothing
+    assert np.array_equal(oracle.paged_attention(q, kc, vc, "f16", tables, lens, 0.3, window=64), full)
+    # window 1: the last key only
+    one = oracle.paged_attention(q, kc, vc, "f16", tables, lens, 0.3, window=1)
+    for i, L in enumerate(lens):
+        assert np.array_equal(one[i], vs[i][L - 1].double().repeat_interleave(2, dim=0).numpy())
+    # a window starting on a block boundary equals full attention over the
+    # table shifted by whole blocks (a different path through the oracle)
+    w = 29  # 45 - 29 = 16: the window starts at block 1 of sequence 0
+    win = oracle.paged_attention(q[:1], kc, vc, "f16", tables[:1], lens[:1], 0.3, window=w)
+    shifted = tables[:1, 1:].clone()
+    alt = oracle.paged_attention(q[:1], kc, vc, "f16", shifted, [w], 0.3)
+    assert np.array_equal(win, alt)
+    # causal chunk rows with a window: row i equals a windowed one-row decode
+    ql, L = 6, 45
+    qq = W.normal(W.generator(41), (ql, 4, 16), 1.0, "f16")
+    chunk = oracle.paged_attention(qq, kc, vc, "f16", tables[:1], [L], 0.3, cu_q=[0, ql], causal=True, window=10)
+    for i in range(ql):
+        one_row = oracle.paged_attention(qq[i:i + 1], kc, vc, "f16", tables[:1], [L - ql + i + 1], 0.3, window=10)
+        assert np.array_equal(chunk[i], one_row[0])
