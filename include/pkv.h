@@ -217,6 +217,31 @@ PKV_API pkv_status pkv_attn_varlen(const void *q, int64_t q_token_stride, const 
                                    int32_t out_dtype, void *workspace, size_t workspace_bytes,
                                    int32_t *err_word, pkv_stream stream);
 
+/* ---- sliding-window variants --------------------------------------------- */
+/*
+ * [P2] "PagedAttention vs sliding-window attention, RadixAttention, and SSMs":
+ * with a sliding window each query attends only to the most recent `window`
+ * tokens, and paged allocation still holds them.  A row whose last visible key
+ * is `last` (L - 1 for a decode row, kv_len - q_len + i for causal chunk row
+ * i, kv_len - 1 without causality) sees keys max(0, last - window + 1) .. last.
+ * Sub-blocks wholly before the window are never read.  window <= 0 means no
+ * window; otherwise arguments, layouts and errors are those of
+ * pkv_attn_decode / pkv_attn_varlen (same workspace sizes).
+ */
+PKV_API pkv_status pkv_attn_decode_window(const void *q, int64_t q_token_stride, const pkv_cache *cache,
+                                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                                          float scale, int32_t window, void *out, int32_t out_dtype,
+                                          void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                          pkv_stream stream);
+PKV_API pkv_status pkv_attn_varlen_window(const void *q, int64_t q_token_stride, const pkv_cache *cache,
+                                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                                          int32_t num_seqs, int32_t total_q, int32_t max_q_len,
+                                          int32_t num_q_heads, float scale, int32_t causal, int32_t window,
+                                          void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                                          int32_t *err_word, pkv_stream stream);
+
 /* ---- a10: block copy for copy-on-write ----------------------------------- */
 /*
  * [P1] Architecture Overview, copy-on-write: when sequences that share a

@@ -119,8 +119,10 @@ def _workspace(size_fn, workspace: Optional[torch.Tensor], device) -> torch.Tens
 def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                 seq_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
                 out_dtype: torch.dtype = torch.float32, workspace: Optional[torch.Tensor] = None,
-                err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """q [B, Hq, D]; tables [B, max_blocks] int32; seq_lens [B] int32 -> out [B, Hq, D]."""
+                err: Optional[torch.Tensor] = None, stream=None, window: int = 0) -> torch.Tensor:
+    """q [B, Hq, D]; tables [B, max_blocks] int32; seq_lens [B] int32 -> out [B, Hq, D].
+
+    window > 0 attends only each sequence's most recent ``window`` keys."""
     c = _cache(k_cache, v_cache)
     _cuda(q, "q")
     _check_i32(block_tables, "block_tables")
@@ -133,10 +135,16 @@ def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
     elif not out.is_contiguous() or out.shape != q.shape:
         raise ValueError("out must be contiguous [B, Hq, D]")
     ws = _workspace(lambda: decode_workspace_size(B, hq, c.num_kv_heads, d, q.device.index), workspace, q.device)
-    check(lib().pkv_attn_decode(_ptr(q), _row_stride(q, "q"), ctypes.byref(c), _ptr(block_tables),
-                                block_tables.shape[1] if block_tables.dim() == 2 else 0, _ptr(seq_lens), B, hq,
-                                float(scale), _ptr(out), _DT[out.dtype], _ptr(ws),
-                                ws.numel() * ws.element_size(), _ptr(err), _stream(stream)))
+    mb = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    if window > 0:
+        check(lib().pkv_attn_decode_window(_ptr(q), _row_stride(q, "q"), ctypes.byref(c), _ptr(block_tables), mb,
+                                           _ptr(seq_lens), B, hq, float(scale), int(window), _ptr(out),
+                                           _DT[out.dtype], _ptr(ws), ws.numel() * ws.element_size(), _ptr(err),
+                                           _stream(stream)))
+    else:
+        check(lib().pkv_attn_decode(_ptr(q), _row_stride(q, "q"), ctypes.byref(c), _ptr(block_tables), mb,
+                                    _ptr(seq_lens), B, hq, float(scale), _ptr(out), _DT[out.dtype], _ptr(ws),
+                                    ws.numel() * ws.element_size(), _ptr(err), _stream(stream)))
     return out
 
 
@@ -144,8 +152,10 @@ def attn_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
                 cu_seqlens_q: torch.Tensor, seq_lens: torch.Tensor, max_q_len: int, scale: float,
                 causal: bool = True, out: Optional[torch.Tensor] = None,
                 out_dtype: torch.dtype = torch.float32, workspace: Optional[torch.Tensor] = None,
-                err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Packed rows q [total_q, Hq, D]; cu_seqlens_q [B+1]; seq_lens = kv_len [B]."""
+                err: Optional[torch.Tensor] = None, stream=None, window: int = 0) -> torch.Tensor:
+    """Packed rows q [total_q, Hq, D]; cu_seqlens_q [B+1]; seq_lens = kv_len [B].
+
+    window > 0 attends only each row's most recent ``window`` keys."""
     c = _cache(k_cache, v_cache)
     _cuda(q, "q")
     _check_i32(block_tables, "block_tables")
@@ -160,10 +170,17 @@ def attn_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
     if out is None:
         out = torch.empty((total, hq, d), dtype=out_dtype, device=q.device)
     ws = _workspace(lambda: varlen_workspace_size(B, hq, c.num_kv_heads, d, q.device.index), workspace, q.device)
-    check(lib().pkv_attn_varlen(_ptr(q), _row_stride(q, "q"), ctypes.byref(c), _ptr(block_tables),
-                                block_tables.shape[1], _ptr(cu_seqlens_q), _ptr(seq_lens), B, total,
-                                int(max_q_len), hq, float(scale), 1 if causal else 0, _ptr(out), _DT[out.dtype],
-                                _ptr(ws), ws.numel() * ws.element_size(), _ptr(err), _stream(stream)))
+    if window > 0:
+        check(lib().pkv_attn_varlen_window(_ptr(q), _row_stride(q, "q"), ctypes.byref(c), _ptr(block_tables),
+                                           block_tables.shape[1], _ptr(cu_seqlens_q), _ptr(seq_lens), B, total,
+                                           int(max_q_len), hq, float(scale), 1 if causal else 0, int(window),
+                                           _ptr(out), _DT[out.dtype], _ptr(ws), ws.numel() * ws.element_size(),
+                                           _ptr(err), _stream(stream)))
+    else:
+        check(lib().pkv_attn_varlen(_ptr(q), _row_stride(q, "q"), ctypes.byref(c), _ptr(block_tables),
+                                    block_tables.shape[1], _ptr(cu_seqlens_q), _ptr(seq_lens), B, total,
+                                    int(max_q_len), hq, float(scale), 1 if causal else 0, _ptr(out), _DT[out.dtype],
+                                    _ptr(ws), ws.numel() * ws.element_size(), _ptr(err), _stream(stream)))
     return out
 
 

@@ -63,6 +63,10 @@ SIGNATURES = {
     "pkv_attn_varlen_workspace_size": (_i32, [_i32, _i32, _i32, _i32, _i32, _P(_sz)]),
     "pkv_attn_varlen": (_i32, [_vp, _i64, _P(PkvCache), _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
                                _f32, _i32, _vp, _i32, _vp, _sz, _vp, _vp]),
+    "pkv_attn_decode_window": (_i32, [_vp, _i64, _P(PkvCache), _vp, _i32, _vp, _i32, _i32, _f32, _i32, _vp,
+                                      _i32, _vp, _sz, _vp, _vp]),
+    "pkv_attn_varlen_window": (_i32, [_vp, _i64, _P(PkvCache), _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
+                                      _f32, _i32, _i32, _vp, _i32, _vp, _sz, _vp, _vp]),
     "pkv_copy_blocks": (_i32, [_P(PkvCache), _i32, _vp, _i32, _vp, _vp]),
     "pkv_check_copy_pairs": (_i32, [_vp, _i32, _i32]),
     "pkv_alloc_create": (_i32, [_i32, _i32, _P(_vp)]),

@@ -60,15 +60,22 @@ struct DecodeParams {
     int32_t cmax;                  // gridDim.x
     int32_t *err;
     int32_t stages;
+    int32_t window;                // > 0: attend only the last `window` keys
 };
 
-// Sub-blocks of sequence s handled by the decode kernel (0 when skipped).
+// First key a decode row of a sequence with L keys attends (sliding window).
+__device__ __forceinline__ int decode_first_key(const DecodeParams &p, int L) {
+    return (p.window > 0 && L > p.window) ? L - p.window : 0;
+}
+
+// Sub-blocks of sequence s handled by the decode kernel (0 when skipped):
+// those from the one holding its first attended key to the one holding L-1.
 __device__ __forceinline__ int decode_sub_blocks(const DecodeParams &p, int s) {
     if (p.cu_q && p.cu_q[s + 1] - p.cu_q[s] != 1) return 0;
     const int L = p.seq_lens[s];
     if (L <= 0) return 0;
     if ((int64_t)L > (int64_t)p.max_blocks * p.block_size) return 0;
-    return (L + kSub - 1) / kSub;
+    return (L + kSub - 1) / kSub - decode_first_key(p, L) / kSub;
 }
 
 __device__ __forceinline__ bool decode_bad_length(const DecodeParams &p, int s) {
@@ -202,11 +209,12 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
             }
             const int b1 = (int)(sb + (hi - x) < n_s ? sb + (hi - x) : n_s);
             const int32_t *trow = p.tables + (int64_t)s * p.max_blocks;
+            const int sb0 = decode_first_key(p, p.seq_lens[s]) / kSub;  // window: first sub-block
             for (int j0 = sb; j0 < b1 && !aborted; j0 += 32) {
                 const int jn = min(32, b1 - j0);
                 int row = 0;
                 if (lane < jn) {
-                    const int tok = (j0 + lane) * kSub;
+                    const int tok = (sb0 + j0 + lane) * kSub;
                     const int lb = tok / p.block_size;
                     int phys = trow[lb];
                     if (phys < 0 || phys >= p.num_blocks) {
@@ -282,6 +290,8 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
         }
         const int b1 = (int)(sb + (hi - x) < n_s ? sb + (hi - x) : n_s);
         const int L = p.seq_lens[s];
+        const int first_key = decode_first_key(p, L);
+        const int sb0 = first_key / kSub;
         const int64_t qrow = p.cu_q ? (int64_t)p.cu_q[s] : (int64_t)s;
 
         // query fragments: B operand (16 dims x 8 heads), head g of the group
@@ -313,7 +323,9 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
             }
             const uint8_t *kb = base + stage * stage_bytes + (w * HALVES) * kTile;
             const uint8_t *vb = kb + tiles * kTile;
-            const int nv = min(kSub, L - j * kSub);
+            const int tok0 = (sb0 + j) * kSub;
+            const int nv = min(kSub, L - tok0);        // tokens below nv are in the sequence
+            const int nlo = first_key - tok0;          // tokens below nlo are outside the window
 
             // S^T[16 tokens x 8 heads] = K q^T
             float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -331,6 +343,10 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
             if (nv < kSub) {
                 if (g >= nv) x0 = x1 = -INFINITY;
                 if (g + 8 >= nv) x2 = x3 = -INFINITY;
+            }
+            if (nlo > 0) {
+                if (g < nlo) x0 = x1 = -INFINITY;
+                if (g + 8 < nlo) x2 = x3 = -INFINITY;
             }
             if (hA >= G) x0 = x2 = 0.f;
             if (hB >= G) x1 = x3 = 0.f;
@@ -662,11 +678,11 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     return PKV_OK;
 }
 
-// Shared by pkv_attn_decode (cu_q == NULL) and pkv_attn_varlen (q_len == 1 rows).
-pkv_status run_decode(const void *q, int64_t q_stride, const pkv_cache *cache, const int32_t *tables,
-                      int32_t max_blocks, const int32_t *seq_lens, const int32_t *cu_q, int32_t num_seqs,
-                      int32_t num_q_heads, float scale, void *out, int32_t out_dtype, void *workspace,
-                      size_t workspace_bytes, int32_t *err_word, cudaStream_t stream) {
+// Shared by pkv_attn_decode[_window] (cu_q == NULL) and pkv_attn_varlen[_window] (q_len == 1 rows).
+pkv_status run_decode_window(const void *q, int64_t q_stride, const pkv_cache *cache, const int32_t *tables,
+                             int32_t max_blocks, const int32_t *seq_lens, const int32_t *cu_q, int32_t num_seqs,
+                             int32_t num_q_heads, float scale, int32_t window, void *out, int32_t out_dtype,
+                             void *workspace, size_t workspace_bytes, int32_t *err_word, cudaStream_t stream) {
     DecodePlan pl;
     pkv_status st = make_plan(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, -1, &pl);
     if (st != PKV_OK) return st;
@@ -703,12 +719,21 @@ pkv_status run_decode(const void *q, int64_t q_stride, const pkv_cache *cache, c
     p.cmax = pl.cmax;
     p.err = err_word;
     p.stages = pl.stages;
+    p.window = window > 0 ? window : 0;
     const bool bf = cache->dtype == PKV_BF16;
     if (cache->head_dim == 64)
         return bf ? launch_decode_t<64, __nv_bfloat16>(mk, mv, p, pl, stream)
                   : launch_decode_t<64, __half>(mk, mv, p, pl, stream);
     return bf ? launch_decode_t<128, __nv_bfloat16>(mk, mv, p, pl, stream)
               : launch_decode_t<128, __half>(mk, mv, p, pl, stream);
+}
+
+pkv_status run_decode(const void *q, int64_t q_stride, const pkv_cache *cache, const int32_t *tables,
+                      int32_t max_blocks, const int32_t *seq_lens, const int32_t *cu_q, int32_t num_seqs,
+                      int32_t num_q_heads, float scale, void *out, int32_t out_dtype, void *workspace,
+                      size_t workspace_bytes, int32_t *err_word, cudaStream_t stream) {
+    return run_decode_window(q, q_stride, cache, tables, max_blocks, seq_lens, cu_q, num_seqs, num_q_heads, scale, 0,
+                             out, out_dtype, workspace, workspace_bytes, err_word, stream);
 }
 
 pkv_status decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, int32_t head_dim,
@@ -764,6 +789,20 @@ pkv_status pkv_attn_decode(const void *q, int64_t q_token_stride, const pkv_cach
     if (num_seqs == 0) return ok();
     st = run_decode(q, q_token_stride, cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
                     num_q_heads, scale, out, out_dtype, workspace, workspace_bytes, err_word, stream);
+    return st == PKV_OK ? ok() : st;
+}
+
+pkv_status pkv_attn_decode_window(const void *q, int64_t q_token_stride, const pkv_cache *cache,
+                                  const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                  int32_t num_seqs, int32_t num_q_heads, float scale, int32_t window, void *out,
+                                  int32_t out_dtype, void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                  pkv_stream stream) {
+    pkv_status st = check_attention_common(q, q_token_stride, cache, block_tables, max_blocks_per_seq, seq_lens,
+                                           num_seqs, num_q_heads, out, out_dtype, "pkv_attn_decode_window");
+    if (st != PKV_OK) return st;
+    if (num_seqs == 0) return ok();
+    st = run_decode_window(q, q_token_stride, cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
+                           num_q_heads, scale, window, out, out_dtype, workspace, workspace_bytes, err_word, stream);
     return st == PKV_OK ? ok() : st;
 }
 

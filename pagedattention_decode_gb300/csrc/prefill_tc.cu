@@ -61,6 +61,7 @@ struct TcParams {
     int32_t out_f32;
     int32_t *err;
     int32_t q_tiles;
+    int32_t window;   // > 0: each row attends only its most recent `window` keys
 };
 
 // UMMA shared-memory descriptor, 128-byte swizzle (sm_100 family layout:
@@ -167,7 +168,11 @@ __global__ void __launch_bounds__(192, 2)
     }
     const int last_row = min(q_len, q0 + R) - 1;
     const int kv_hi = p.causal ? kv_len - q_len + last_row + 1 : kv_len;
-    const int nt = (kv_hi + kTok - 1) / kTok;
+    // window: the CTA's first row has the lowest first key of its rows
+    const int lim_first = p.causal ? kv_len - q_len + q0 : kv_len - 1;
+    const int lo_first = (p.window > 0 && lim_first - p.window + 1 > 0) ? lim_first - p.window + 1 : 0;
+    const int j_first = lo_first / kTok;
+    const int nt = (kv_hi + kTok - 1) / kTok - j_first;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
@@ -225,7 +230,7 @@ __global__ void __launch_bounds__(192, 2)
                 }
                 break;
             }
-            const int t0 = j * kTok;
+            const int t0 = (j_first + j) * kTok;
             const int nvalid = min(kTok, kv_len - t0);
             const int nsub = (nvalid + 15) / 16;
             if (lane == 0) mbar_arrive_expect_tx(&kv_full[stage], (uint32_t)(nsub * 2 * HALVES * 2048));
@@ -305,6 +310,7 @@ __global__ void __launch_bounds__(192, 2)
         const int qi = q0 + row % R;
         const bool valid = qi < q_len;
         const int lim = (p.causal && valid) ? kv_len - q_len + qi : kv_len - 1;
+        const int lo = (p.window > 0 && lim - p.window + 1 > 0) ? lim - p.window + 1 : 0;
         const float sl = p.scale_log2;
         float m_used = -INFINITY, lsum = 0.f;
         bool ok = true;
@@ -320,13 +326,13 @@ __global__ void __launch_bounds__(192, 2)
             tmem_ld32(trow_addr + b * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
             tmem_ld32(trow_addr + b * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
             tmem_wait_ld();
-            const int t0 = j * kTok;
+            const int t0 = (j_first + j) * kTok;
             // eight independent partial maxima (short dependency chains);
             // tiles every row of the warp sees in full skip the causal select
             float pm[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
-            if (__all_sync(0xffffffffu, t0 + kTok - 1 <= lim)) {
+            if (__all_sync(0xffffffffu, t0 + kTok - 1 <= lim && t0 >= lo)) {
 #pragma unroll
                 for (int c = 0; c < kTok; ++c) {
                     const float x = __uint_as_float(sr[c]) * sl;
@@ -336,7 +342,7 @@ __global__ void __launch_bounds__(192, 2)
             } else {
 #pragma unroll
                 for (int c = 0; c < kTok; ++c) {
-                    const float x = (t0 + c <= lim) ? __uint_as_float(sr[c]) * sl : -INFINITY;
+                    const float x = (t0 + c <= lim && t0 + c >= lo) ? __uint_as_float(sr[c]) * sl : -INFINITY;
                     sr[c] = __float_as_uint(x);
                     pm[c & 7] = fmaxf(pm[c & 7], x);
                 }
@@ -372,10 +378,17 @@ __global__ void __launch_bounds__(192, 2)
             float ps[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) ps[u] = 0.f;
+            // with a window a row can meet whole tiles before its first key:
+            // there m_used is still -inf and those p must be 0, not NaN
+            const bool none_yet = m_used == -INFINITY;
 #pragma unroll
             for (int c = 0; c < kTok; c += 2) {
-                const float p0 = fast_exp2(__uint_as_float(sr[c]) - m_used);
-                const float p1 = fast_exp2(__uint_as_float(sr[c + 1]) - m_used);
+                float p0 = fast_exp2(__uint_as_float(sr[c]) - m_used);
+                float p1 = fast_exp2(__uint_as_float(sr[c + 1]) - m_used);
+                if (none_yet) {
+                    p0 = 0.f;
+                    p1 = 0.f;
+                }
                 ps[(c >> 1) & 7] += p0 + p1;
                 const uint32_t h = pack2<T>(p0, p1);
                 const float2 hf = unpack2<T>(h);
@@ -472,7 +485,7 @@ static pkv_status launch_prefill_tc_t(const CUtensorMap &mq, const CUtensorMap &
 pkv_status run_prefill_tc(const void *q, int64_t q_stride, const pkv_cache *cache, const int32_t *tables,
                           int32_t max_blocks, const int32_t *cu_q, const int32_t *seq_lens, int32_t num_seqs,
                           int32_t total_q, int32_t max_q_len, int32_t num_q_heads, float scale, int32_t causal,
-                          void *out, int32_t out_dtype, int32_t *err_word, cudaStream_t stream) {
+                          int32_t window, void *out, int32_t out_dtype, int32_t *err_word, cudaStream_t stream) {
     PKV_CHECK_ARG(aligned16(q) && (q_stride * 2) % 16 == 0, PKV_ERR_INVALID_ARG,
                   "pkv_attn_varlen: q and its row stride must be 16-byte aligned for prefill chunks");
     TcParams p{};
@@ -489,6 +502,7 @@ pkv_status run_prefill_tc(const void *q, int64_t q_stride, const pkv_cache *cach
     p.out = out;
     p.out_f32 = out_dtype == PKV_F32;
     p.err = err_word;
+    p.window = window > 0 ? window : 0;
     const int rows = 128 / p.group;
     p.q_tiles = (max_q_len + rows - 1) / rows;
     CUtensorMap mq, mk, mv;

@@ -174,3 +174,29 @@ def test_full_size_workload_sampled(wl):
         case = PagedCase(q[i:i + 1], ksub, vsub, torch.arange(nbk, dtype=torch.int32).view(1, -1),
                          lens[i:i + 1], w.scale, w.dtype)
         assert_close(out[i:i + 1], case.oracle(), what=f"{w.name} seq {i}")
+
+
+@pytest.mark.parametrize("window", [1, 15, 16, 17, 100, 4096])
+@pytest.mark.parametrize("hq,hkv,d,bs,dtype", [(32, 8, 128, 16, "f16"), (12, 12, 64, 32, "bf16")])
+def test_sliding_window_decode(window, hq, hkv, d, bs, dtype):
+    lens = [1, 15, 16, 17, 0, 33, 300, 1000, 2500]
+    case = decode_case(60 + window, lens, hq, hkv, d, bs, dtype, sigma=1.0 if dtype == "f16" else 0.5)
+    c = case.to("cuda")
+    got = P.attn_decode(c.q, c.k_cache, c.v_cache, c.tables, c.lens, c.scale, window=window)
+    torch.cuda.synchronize()
+    want = oracle_window(case, window)
+    assert_close(got, want, what=f"window {window}")
+
+
+def oracle_window(case, window):
+    import oracle
+    return oracle.paged_attention(case.q, case.k_cache, case.v_cache, case.dtype, case.tables.numpy(),
+                                  case.lens.numpy(), case.scale, window=window)
+
+
+def test_sliding_window_long_sequence_split():
+    case = decode_case(70, [40000, 7, 9000], 32, 8, 128, 16, "bf16", sigma=0.5)
+    c = case.to("cuda")
+    got = P.attn_decode(c.q, c.k_cache, c.v_cache, c.tables, c.lens, c.scale, window=4097)
+    torch.cuda.synchronize()
+    assert_close(got, oracle_window(case, 4097), what="window 4097")

@@ -64,3 +64,19 @@ def test_q_len_beyond_kv_len_is_flagged():
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     run(case, err=err)
     assert int(err.item()) & P.DEVERR["length"]
+
+
+@pytest.mark.parametrize("window", [1, 33, 64, 200])
+@pytest.mark.parametrize("causal", [True, False])
+def test_sliding_window_varlen(window, causal):
+    import oracle
+    q_lens = [77, 1, 300, 1, 2, 130]
+    kv_lens = [77 + 200, 50, 300, 1, 2, 1000]
+    case = varlen_case(80 + window, q_lens, kv_lens, 32, 8, 128, 16)
+    c = case.to("cuda")
+    out = P.attn_varlen(c.q, c.k_cache, c.v_cache, c.tables, c.cu_q, c.lens, max(q_lens), c.scale, causal=causal,
+                        window=window)
+    torch.cuda.synchronize()
+    want = oracle.paged_attention(case.q, case.k_cache, case.v_cache, case.dtype, case.tables.numpy(),
+                                  case.lens.numpy(), case.scale, cu_q=case.cu_q.numpy(), causal=causal, window=window)
+    assert_close(out, want, what=f"varlen window {window} causal {causal}")
