@@ -331,6 +331,34 @@ PKV_API pkv_status pkv_seq_block_table(const pkv_allocator *a, int32_t seq_id, i
 PKV_API pkv_status pkv_seq_fill_tables(const pkv_allocator *a, const int32_t *seq_ids, int32_t n,
                                        int32_t *tables, int32_t max_blocks, int32_t *seq_lens);
 
+/*
+ * Prefix sharing ([P1] Step 4, the radix/prefix tree, and Step 2's LRU
+ * reclaim).  The trie's children are keyed by one whole block of token ids
+ * (only whole blocks are shared).
+ *  - pkv_prefix_match walks `tokens` block by block and writes the ids of the
+ *    matched blocks (at most `capacity`); it does not retain them: passing them
+ *    to pkv_seq_create retains each once ([P1]'s listing retains twice).  With
+ *    other threads evicting, use pkv_seq_create_prefixed instead.
+ *  - pkv_prefix_insert publishes the whole blocks of a sequence (block_ids[j]
+ *    holds tokens j*block_size .. j*block_size + block_size - 1); a new node
+ *    takes one reference to its block; an existing key keeps its block.
+ *  - pkv_prefix_evict removes up to max_blocks least recently used leaves whose
+ *    block is held by the trie alone, releasing those blocks to the free stack;
+ *    out_ids gets them in eviction order.
+ * Recency is a logical clock advanced by each node a match or insert touches.
+ */
+PKV_API pkv_status pkv_prefix_match(pkv_allocator *a, const int32_t *tokens, int64_t num_tokens, int32_t *out_ids,
+                                    int32_t capacity, int32_t *num_blocks);
+/* Match and create in one step (under the allocator's lock, so no eviction can
+ * come between them): a new sequence holding the matched whole blocks of
+ * `tokens`, each retained once; *shared_tokens gets its length. */
+PKV_API pkv_status pkv_seq_create_prefixed(pkv_allocator *a, const int32_t *tokens, int64_t num_tokens,
+                                           int32_t *seq_id, int64_t *shared_tokens);
+PKV_API pkv_status pkv_prefix_insert(pkv_allocator *a, const int32_t *tokens, int64_t num_tokens,
+                                     const int32_t *block_ids, int32_t num_ids);
+PKV_API pkv_status pkv_prefix_evict(pkv_allocator *a, int32_t max_blocks, int32_t *out_ids, int32_t *num_evicted);
+PKV_API int32_t pkv_prefix_num_nodes(const pkv_allocator *a);
+
 #ifdef __cplusplus
 }
 #endif

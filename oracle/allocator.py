@@ -35,6 +35,15 @@ Readings where the pages are silent or at odds (each listed in the design doc):
   new block ``dst``, records the pair (tail, dst), releases the tail and writes
   into ``dst``; the last holder (refcount 1) writes in place; a full tail
   needs no copy.  Page 1's listing never copies (a bug).
+* prefix trie (page 1, Step 4, and the LRU reclaim of Step 2): children are
+  keyed by a whole block of token ids; ``prefix_match`` walks whole blocks and
+  returns their ids without retaining them (the new sequence retains each
+  once when it is created -- page 1 retains twice); ``prefix_insert``
+  publishes a sequence's whole blocks, the trie holding one reference to each
+  node's block (first writer wins on an existing key); ``prefix_evict``
+  removes least recently used leaves whose block only the trie still holds
+  and releases them.  Recency is a logical clock bumped by every match or
+  insert that touches a node.
 """
 
 from __future__ import annotations
@@ -50,6 +59,18 @@ class DoubleFree(ValueError):
     """An id that is not handed out was freed (page 3's ValueError)."""
 
 
+class _Node:
+    __slots__ = ("children", "block", "last_used", "parent", "key", "serial")
+
+    def __init__(self, parent=None, key=None, block=-1, serial=0):
+        self.children = {}
+        self.block = block
+        self.last_used = 0
+        self.parent = parent
+        self.key = key
+        self.serial = serial
+
+
 class RefAllocator:
     def __init__(self, num_blocks: int, block_size: int):
         if num_blocks <= 0 or block_size <= 0:
@@ -63,6 +84,10 @@ class RefAllocator:
         self.freed: set = set()
         self.next_seq = 0
         self.stats = {"allocs": 0, "frees": 0, "cow_copies": 0, "peak_used": 0}
+        self.root = _Node()
+        self.clock = 0
+        self.node_serial = 0
+        self.nodes = 0
 
     # ---- block level -------------------------------------------------------
     @property
@@ -228,6 +253,68 @@ class RefAllocator:
     def seq_len(self, sid: int) -> int:
         return self.lens[sid]
 
+    # ---- prefix trie -------------------------------------------------------
+    def _tick(self) -> int:
+        self.clock += 1
+        return self.clock
+
+    def prefix_match(self, tokens: Sequence[int]) -> List[int]:
+        bs = self.block_size
+        node, ids = self.root, []
+        for j in range(len(tokens) // bs):
+            key = tuple(int(t) for t in tokens[j * bs:(j + 1) * bs])
+            child = node.children.get(key)
+            if child is None:
+                break
+            node = child
+            node.last_used = self._tick()
+            ids.append(node.block)
+        return ids
+
+    def create_sequence_prefixed(self, tokens: Sequence[int]) -> Tuple[int, int]:
+        shared = self.prefix_match(tokens)
+        sid = self.create_sequence(shared, len(shared) * self.block_size)
+        return sid, len(shared) * self.block_size
+
+    def prefix_insert(self, tokens: Sequence[int], block_ids: Sequence[int]) -> None:
+        bs = self.block_size
+        n = min(len(block_ids), len(tokens) // bs)
+        for j in range(n):
+            if block_ids[j] not in self.refcount:
+                raise DoubleFree(f"block {block_ids[j]} is not allocated")
+        node = self.root
+        for j in range(n):
+            key = tuple(int(t) for t in tokens[j * bs:(j + 1) * bs])
+            child = node.children.get(key)
+            if child is None:
+                self.node_serial += 1
+                child = _Node(node, key, int(block_ids[j]), self.node_serial)
+                node.children[key] = child
+                self.retain(child.block)
+                self.nodes += 1
+            node = child
+            node.last_used = self._tick()
+
+    def prefix_evict(self, max_blocks: int) -> List[int]:
+        evicted: List[int] = []
+        while len(evicted) < max_blocks:
+            best = None
+            stack = list(self.root.children.values())
+            while stack:
+                nd = stack.pop()
+                if nd.children:
+                    stack.extend(nd.children.values())
+                elif self.refcount.get(nd.block) == 1:
+                    if best is None or (nd.last_used, nd.serial) < (best.last_used, best.serial):
+                        best = nd
+            if best is None:
+                break
+            del best.parent.children[best.key]
+            self.nodes -= 1
+            self.release(best.block)
+            evicted.append(best.block)
+        return evicted
+
     def check_invariants(self, exact: bool = True) -> None:
         """Every id is in exactly one of {free stack, handed out}; refcounts
         equal (``exact``) or exceed the number of table entries holding the id
@@ -240,6 +327,11 @@ class RefAllocator:
         for t in self.tables.values():
             for b in t:
                 held[b] = held.get(b, 0) + 1
+        stack = list(self.root.children.values())
+        while stack:
+            nd = stack.pop()
+            stack.extend(nd.children.values())
+            held[nd.block] = held.get(nd.block, 0) + 1
         for b, c in held.items():
             rc = self.refcount.get(b, 0)
             assert rc >= c, f"refcount of {b} is {rc}, held {c}"

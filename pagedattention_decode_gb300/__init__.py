@@ -316,6 +316,40 @@ class BlockAllocator:
         check(lib().pkv_seq_block_table(self._h, seq_id, buf, cap, ctypes.byref(n)))
         return list(buf[:n.value])
 
+    # prefix sharing
+    def prefix_match(self, tokens: Sequence[int]) -> List[int]:
+        """Ids of the whole blocks of ``tokens`` already in the trie (not retained)."""
+        n = len(tokens)
+        toks = (ctypes.c_int32 * max(1, n))(*tokens)
+        cap = n // self.block_size
+        out = (ctypes.c_int32 * max(1, cap))()
+        m = ctypes.c_int32()
+        check(lib().pkv_prefix_match(self._h, toks, n, out, cap, ctypes.byref(m)))
+        return list(out[:m.value])
+
+    def create_sequence_prefixed(self, tokens: Sequence[int]) -> Tuple[int, int]:
+        """New sequence on the trie's matched whole blocks of ``tokens`` (match and
+        create atomically); returns (sequence id, shared token count)."""
+        toks = (ctypes.c_int32 * max(1, len(tokens)))(*tokens)
+        sid, shared = ctypes.c_int32(), ctypes.c_int64()
+        check(lib().pkv_seq_create_prefixed(self._h, toks, len(tokens), ctypes.byref(sid), ctypes.byref(shared)))
+        return sid.value, shared.value
+
+    def prefix_insert(self, tokens: Sequence[int], block_ids: Sequence[int]) -> None:
+        toks = (ctypes.c_int32 * max(1, len(tokens)))(*tokens)
+        ids = (ctypes.c_int32 * max(1, len(block_ids)))(*block_ids)
+        check(lib().pkv_prefix_insert(self._h, toks, len(tokens), ids, len(block_ids)))
+
+    def prefix_evict(self, max_blocks: int) -> List[int]:
+        out = (ctypes.c_int32 * max(1, max_blocks))()
+        n = ctypes.c_int32()
+        check(lib().pkv_prefix_evict(self._h, max_blocks, out, ctypes.byref(n)))
+        return list(out[:n.value])
+
+    @property
+    def prefix_nodes(self) -> int:
+        return lib().pkv_prefix_num_nodes(self._h)
+
     def fill_tables(self, seq_ids: Sequence[int], max_blocks: int, tables_out: torch.Tensor,
                     lens_out: torch.Tensor) -> None:
         """Rows of tables_out [n, max_blocks] int32 and lens_out [n] int32 (CPU tensors)."""

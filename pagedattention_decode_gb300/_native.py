@@ -88,6 +88,11 @@ SIGNATURES = {
     "pkv_seq_len": (_i32, [_vp, _i32, _P(_i64)]),
     "pkv_seq_block_table": (_i32, [_vp, _i32, _vp, _i32, _P(_i32)]),
     "pkv_seq_fill_tables": (_i32, [_vp, _vp, _i32, _vp, _i32, _vp]),
+    "pkv_prefix_match": (_i32, [_vp, _vp, _i64, _vp, _i32, _P(_i32)]),
+    "pkv_seq_create_prefixed": (_i32, [_vp, _vp, _i64, _P(_i32), _P(_i64)]),
+    "pkv_prefix_insert": (_i32, [_vp, _vp, _i64, _vp, _i32]),
+    "pkv_prefix_evict": (_i32, [_vp, _i32, _vp, _P(_i32)]),
+    "pkv_prefix_num_nodes": (_i32, [_vp]),
 }
 
 _lib = None

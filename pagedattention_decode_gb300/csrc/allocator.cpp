@@ -16,6 +16,7 @@
 // copy-on-write paragraph: refcounts (1 on allocation, +1 per share/fork),
 // forks share every id, a shared block is copied on the first divergent write.
 #include <algorithm>
+#include <map>
 #include <mutex>
 #include <unordered_map>
 #include <vector>
@@ -35,6 +36,21 @@ struct pkv_allocator {
     std::vector<Seq> seqs;
     pkv_alloc_counters counters{0, 0, 0, 0};
     mutable std::mutex mu;
+
+    // Prefix trie ("Build a paged KV cache manager from scratch", Step 4):
+    // children keyed by one whole block of token ids; each node holds one
+    // reference to its block.  Node 0 is the root.
+    struct Node {
+        std::map<std::vector<int32_t>, int32_t> children;
+        int32_t parent = -1;
+        std::vector<int32_t> key;
+        int32_t block = -1;
+        int64_t last_used = 0;
+        bool live = true;
+    };
+    std::vector<Node> nodes{Node{}};
+    int64_t clock = 0;
+    int32_t trie_nodes = 0;
 
     int32_t used() const { return num_blocks - (int32_t)free_stack.size(); }
 
@@ -333,6 +349,119 @@ pkv_status pkv_seq_fill_tables(const pkv_allocator *a, const int32_t *seq_ids, i
         seq_lens[i] = (int32_t)s.len;
     }
     return pkv::ok();
+}
+
+// ---- prefix trie + LRU reclaim ----------------------------------------------
+
+pkv_status pkv_prefix_match(pkv_allocator *a, const int32_t *tokens, int64_t num_tokens, int32_t *out_ids,
+                            int32_t capacity, int32_t *num_blocks) {
+    PKV_CHECK_ARG(a && num_blocks && num_tokens >= 0 && (tokens || num_tokens == 0) && capacity >= 0 &&
+                      (out_ids || capacity == 0),
+                  PKV_ERR_INVALID_ARG, "bad argument");
+    Guard g(a->mu);
+    const int32_t bs = a->block_size;
+    int32_t node = 0, n = 0;
+    std::vector<int32_t> key(bs);
+    for (int64_t j = 0; (j + 1) * bs <= num_tokens && n < capacity; ++j) {
+        std::copy(tokens + j * bs, tokens + (j + 1) * bs, key.begin());
+        auto it = a->nodes[node].children.find(key);
+        if (it == a->nodes[node].children.end()) break;
+        node = it->second;
+        a->nodes[node].last_used = ++a->clock;
+        out_ids[n++] = a->nodes[node].block;
+    }
+    *num_blocks = n;
+    return pkv::ok();
+}
+
+pkv_status pkv_seq_create_prefixed(pkv_allocator *a, const int32_t *tokens, int64_t num_tokens, int32_t *seq_id,
+                                  int64_t *shared_tokens) {
+    PKV_CHECK_ARG(a && seq_id && shared_tokens && num_tokens >= 0 && (tokens || num_tokens == 0),
+                  PKV_ERR_INVALID_ARG, "bad argument");
+    Guard g(a->mu);
+    const int32_t bs = a->block_size;
+    int32_t node = 0;
+    pkv_allocator::Seq sq;
+    std::vector<int32_t> key(bs);
+    for (int64_t j = 0; (j + 1) * bs <= num_tokens; ++j) {
+        std::copy(tokens + j * bs, tokens + (j + 1) * bs, key.begin());
+        auto it = a->nodes[node].children.find(key);
+        if (it == a->nodes[node].children.end()) break;
+        node = it->second;
+        a->nodes[node].last_used = ++a->clock;
+        sq.table.push_back(a->nodes[node].block);
+    }
+    for (int32_t id : sq.table) a->refcount[id] += 1;  // one retain per share
+    sq.len = (int64_t)sq.table.size() * bs;
+    *shared_tokens = sq.len;
+    a->seqs.push_back(std::move(sq));
+    *seq_id = (int32_t)a->seqs.size() - 1;
+    return pkv::ok();
+}
+
+pkv_status pkv_prefix_insert(pkv_allocator *a, const int32_t *tokens, int64_t num_tokens, const int32_t *block_ids,
+                             int32_t num_ids) {
+    PKV_CHECK_ARG(a && num_tokens >= 0 && num_ids >= 0 && (tokens || num_tokens == 0) && (block_ids || num_ids == 0),
+                  PKV_ERR_INVALID_ARG, "bad argument");
+    Guard g(a->mu);
+    const int32_t bs = a->block_size;
+    const int64_t n = std::min<int64_t>(num_ids, num_tokens / bs);
+    for (int64_t j = 0; j < n; ++j)
+        PKV_CHECK_ARG(a->valid_id(block_ids[j]) && a->refcount[block_ids[j]] > 0, PKV_ERR_DOUBLE_FREE,
+                      "block %d is not handed out", block_ids[j]);
+    int32_t node = 0;
+    for (int64_t j = 0; j < n; ++j) {
+        std::vector<int32_t> key(tokens + j * bs, tokens + (j + 1) * bs);
+        auto it = a->nodes[node].children.find(key);
+        int32_t child;
+        if (it == a->nodes[node].children.end()) {
+            pkv_allocator::Node nd;
+            nd.parent = node;
+            nd.key = key;
+            nd.block = block_ids[j];
+            a->nodes.push_back(std::move(nd));
+            child = (int32_t)a->nodes.size() - 1;
+            a->nodes[node].children.emplace(std::move(key), child);
+            a->refcount[block_ids[j]] += 1;  // the trie's own reference
+            a->trie_nodes += 1;
+        } else {
+            child = it->second;  // first writer wins
+        }
+        node = child;
+        a->nodes[node].last_used = ++a->clock;
+    }
+    return pkv::ok();
+}
+
+pkv_status pkv_prefix_evict(pkv_allocator *a, int32_t max_blocks, int32_t *out_ids, int32_t *num_evicted) {
+    PKV_CHECK_ARG(a && num_evicted && max_blocks >= 0 && (out_ids || max_blocks == 0), PKV_ERR_INVALID_ARG,
+                  "bad argument");
+    Guard g(a->mu);
+    int32_t n = 0;
+    while (n < max_blocks) {
+        // least recently used leaf whose block only the trie still holds (ties: oldest node)
+        int32_t best = -1;
+        for (int32_t i = 1; i < (int32_t)a->nodes.size(); ++i) {
+            const auto &nd = a->nodes[i];
+            if (!nd.live || !nd.children.empty() || a->refcount[nd.block] != 1) continue;
+            if (best < 0 || nd.last_used < a->nodes[best].last_used) best = i;
+        }
+        if (best < 0) break;
+        auto &nd = a->nodes[best];
+        a->nodes[nd.parent].children.erase(nd.key);
+        nd.live = false;
+        a->trie_nodes -= 1;
+        a->release_one(nd.block);
+        out_ids[n++] = nd.block;
+    }
+    *num_evicted = n;
+    return pkv::ok();
+}
+
+int32_t pkv_prefix_num_nodes(const pkv_allocator *a) {
+    if (!a) return -1;
+    Guard g(a->mu);
+    return a->trie_nodes;
 }
 
 pkv_status pkv_check_copy_pairs(const int64_t *p, int32_t num_pairs, int32_t num_blocks) {

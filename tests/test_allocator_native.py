@@ -189,3 +189,101 @@ def test_threaded_stress():
     assert all(a.refcount(b) == 0 for b in range(nb))
     c = a.counters()
     assert c["allocs"] == c["frees"]
+
+
+def test_prefix_trie_differential():
+    """Prompts drawn from a few shared system prefixes: match -> create ->
+    append -> insert -> finish, with LRU evictions, op by op against the
+    reference allocator."""
+    rng = random.Random(11)
+    nb, bs = 96, 4
+    n, r = P.BlockAllocator(nb, bs), RefAllocator(nb, bs)
+    prefixes = [[rng.randint(0, 5) for _ in range(rng.randint(4, 16))] for _ in range(4)]
+    live = []
+    for step in range(600):
+        op = rng.random()
+        if op < 0.45:
+            toks = rng.choice(prefixes) + [rng.randint(0, 5) for _ in range(rng.randint(0, 9))]
+            if rng.random() < 0.5:
+                shared = r.prefix_match(toks)
+                assert n.prefix_match(toks) == shared
+                sid = r.create_sequence(shared, len(shared) * bs)
+                assert n.create_sequence(shared, len(shared) * bs) == sid
+            else:
+                sid, stoks = r.create_sequence_prefixed(toks)
+                assert n.create_sequence_prefixed(toks) == (sid, stoks)
+                shared = r.block_table(sid)
+            rest = len(toks) - len(shared) * bs
+            try:
+                want = r.append_tokens([sid], [rest])
+            except Exhausted:
+                with pytest.raises(P.ExhaustedError):
+                    n.append_tokens([sid], [rest])
+                r.free_sequence(sid)
+                n.free_sequence(sid)
+                continue
+            assert n.append_tokens([sid], [rest]) == want
+            r.prefix_insert(toks, r.block_table(sid))
+            n.prefix_insert(toks, n.block_table(sid))
+            live.append(sid)
+        elif op < 0.75 and live:
+            sid = live.pop(rng.randrange(len(live)))
+            r.free_sequence(sid)
+            n.free_sequence(sid)
+        else:
+            k = rng.randint(0, 6)
+            assert n.prefix_evict(k) == r.prefix_evict(k)
+        if step % 25 == 0:
+            _same_state(n, r, live)
+            assert n.prefix_nodes == r.nodes
+            r.check_invariants()
+    for sid in live:
+        r.free_sequence(sid)
+        n.free_sequence(sid)
+    assert n.prefix_evict(nb) == r.prefix_evict(nb)
+    assert n.num_free == r.num_free == nb and n.prefix_nodes == 0
+
+
+def test_prefix_threaded_stress():
+    """'Build a paged KV cache manager from scratch', roadmap item 5: many
+    threads share prefixes, fork, finish and evict concurrently; at the end,
+    after a full eviction, every block is free again."""
+    nb, bs = 1024, 8
+    a = P.BlockAllocator(nb, bs)
+    base = [[t % 7 for t in range(64)], [t % 5 for t in range(40)]]
+    errors = []
+
+    def worker(seed):
+        rng = random.Random(seed)
+        mine = []
+        try:
+            for _ in range(300):
+                op = rng.random()
+                try:
+                    if op < 0.4:
+                        toks = rng.choice(base)[:rng.randint(8, 40)] + [rng.randint(0, 9) for _ in range(5)]
+                        s, shared = a.create_sequence_prefixed(toks)
+                        mine.append(s)
+                        a.append_tokens([s], [len(toks) - shared])
+                        a.prefix_insert(toks, a.block_table(s))
+                    elif op < 0.55 and mine:
+                        mine.append(a.fork(rng.choice(mine)))
+                    elif op < 0.85 and mine:
+                        a.free_sequence(mine.pop(rng.randrange(len(mine))))
+                    else:
+                        a.prefix_evict(rng.randint(1, 8))
+                except P.ExhaustedError:
+                    pass
+            for s in mine:
+                a.free_sequence(s)
+        except Exception as e:  # noqa: BLE001
+            errors.append(e)
+
+    ts = [threading.Thread(target=worker, args=(i,)) for i in range(16)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors
+    a.prefix_evict(nb)
+    assert a.prefix_nodes == 0 and a.num_free == nb

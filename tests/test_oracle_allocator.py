@@ -192,3 +192,78 @@ def test_random_ops_keep_invariants():
     for s in live:
         a.free_sequence(s)
     assert a.num_free == 64 and not a.refcount
+
+
+def test_prefix_sharing_first_block():
+    """Page 1, test_prefix_sharing: two prompts that agree on their first 16
+    tokens share the first block id."""
+    a = RefAllocator(16, 16)
+    p1 = list(range(1, 17)) + [99]
+    p2 = list(range(1, 17)) + [100]
+    s1 = a.create_sequence()
+    a.append_tokens([s1], [len(p1)])
+    a.prefix_insert(p1, a.block_table(s1))
+    shared = a.prefix_match(p2)
+    assert shared == a.block_table(s1)[:1]
+    s2 = a.create_sequence(shared, len(shared) * 16)
+    a.append_tokens([s2], [len(p2) - 16])
+    assert a.block_table(s1)[0] == a.block_table(s2)[0]
+    # one retain per holder: s1, the trie and s2 (page 1 would count it twice for s2)
+    assert a.get_refcount(shared[0]) == 3
+    a.check_invariants()
+    a.free_sequence(s1)
+    a.free_sequence(s2)
+    a.check_invariants()
+
+
+def test_prefix_demo_prompts_share_leading_block():
+    """Page 1's demo: 'The capital of France is' and '... is Paris' share their
+    leading 16-token block; 'The capital of Germany is' shares none at bs 16."""
+    a = RefAllocator(16, 16)
+    prompts = ["The capital of France is", "The capital of France is Paris", "The capital of Germany is"]
+    firsts = []
+    for p in prompts:
+        toks = [ord(c) for c in p]
+        shared = a.prefix_match(toks)
+        s = a.create_sequence(shared, len(shared) * 16)
+        a.append_tokens([s], [len(toks) - len(shared) * 16])
+        a.prefix_insert(toks, a.block_table(s))
+        firsts.append(a.block_table(s)[0])
+        a.free_sequence(s)
+    assert firsts[0] == firsts[1] and firsts[2] != firsts[0]
+    assert a.num_free > 0
+    a.check_invariants()
+
+
+def test_lru_eviction_order_and_reuse():
+    """Page 1, Step 2 (reclaim) and test_eviction_recycles_zero_refcount: once no
+    sequence holds a block, the least recently used one is reclaimed first."""
+    a = RefAllocator(4, 4)
+    sA, sB = a.create_sequence(), a.create_sequence()
+    a.append_tokens([sA, sB], [4, 4])
+    tA, tB = [1, 2, 3, 4], [5, 6, 7, 8]
+    bA, bB = a.block_table(sA)[0], a.block_table(sB)[0]
+    a.prefix_insert(tA, [bA])
+    a.prefix_insert(tB, [bB])
+    a.free_sequence(sA)
+    a.free_sequence(sB)
+    assert a.num_free == 2          # the trie still holds both blocks
+    assert a.prefix_match(tA) == [bA]  # A becomes the most recently used
+    assert a.prefix_evict(1) == [bB]
+    assert a.prefix_match(tB) == [] and a.prefix_match(tA) == [bA]
+    assert a.num_free == 3
+    assert a.prefix_evict(5) == [bA] and a.num_free == 4
+    a.check_invariants()
+
+
+def test_evict_takes_leaves_first_and_skips_blocks_in_use():
+    a = RefAllocator(8, 4)
+    s = a.create_sequence()
+    a.append_tokens([s], [8])
+    b0, b1 = a.block_table(s)
+    a.prefix_insert(list(range(8)), [b0, b1])
+    assert a.prefix_evict(4) == []  # s still holds both
+    a.free_sequence(s)
+    assert a.prefix_evict(4) == [b1, b0]  # the leaf goes first, then its parent
+    assert a.num_free == 8
+    a.check_invariants()
