@@ -68,6 +68,11 @@ def lib():
         L.oracle_paged_attention.argtypes = [vp, i64, vp, vp, i32, i64, i32, i32, i32,
                                              vp, i32, vp, vp, i32, i32,
                                              ctypes.c_double, i32, i32, vp]
+        L.oracle_write_kv_int8.restype = i32
+        L.oracle_write_kv_int8.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp, vp, vp, i64, i32]
+        L.oracle_paged_attention_int8.restype = i32
+        L.oracle_paged_attention_int8.argtypes = [vp, i64, i32, vp, vp, vp, vp, i64, i32, i32, i32,
+                                                  vp, i32, vp, i32, i32, ctypes.c_double, i32, vp]
         _lib = L
     return _lib
 
@@ -159,3 +164,37 @@ def decode_f16(bits: int) -> float:
 
 def decode_bf16(bits: int) -> float:
     return lib().oracle_decode_bf16(bits)
+
+
+def write_kv_int8(k, v, dtype, slots, kq: np.ndarray, vq: np.ndarray, kscale: np.ndarray,
+                  vscale: np.ndarray) -> None:
+    """Quantised write (in place): int8 pools [nb, bs, Hkv, D], float32 scales [nb, Hkv]."""
+    kb, vb = _bits(k), _bits(v)
+    for a, dt in ((kq, np.int8), (vq, np.int8), (kscale, np.float32), (vscale, np.float32)):
+        assert a.dtype == dt and a.flags.c_contiguous
+    T, hkv, d = kb.shape
+    nb, bs = kq.shape[:2]
+    sl = np.ascontiguousarray(np.asarray(slots, dtype=np.int64))
+    rc = lib().oracle_write_kv_int8(_ptr(kb), _ptr(vb), dtype_code(dtype), T, hkv, d, _ptr(sl), _ptr(kq),
+                                    _ptr(vq), _ptr(kscale), _ptr(vscale), nb, bs)
+    if rc != 0:
+        raise ValueError("slot outside the pool")
+
+
+def paged_attention_int8(q, dtype, kq: np.ndarray, vq: np.ndarray, kscale: np.ndarray, vscale: np.ndarray,
+                         block_tables, kv_lens, scale: float, window: int = 0) -> np.ndarray:
+    """binary64 decode attention over an int8 cache (values = code * scale)."""
+    qb = _bits(q)
+    B, hq, d = qb.shape
+    nb, bs, hkv, d2 = kq.shape
+    assert d2 == d
+    tables = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    lens = np.ascontiguousarray(np.asarray(kv_lens, dtype=np.int32))
+    out = np.zeros((B, hq, d), dtype=np.float64)
+    rc = lib().oracle_paged_attention_int8(_ptr(qb), hq * d, dtype_code(dtype), _ptr(np.ascontiguousarray(kq)),
+                                           _ptr(np.ascontiguousarray(vq)), _ptr(np.ascontiguousarray(kscale)),
+                                           _ptr(np.ascontiguousarray(vscale)), nb, bs, hkv, d, _ptr(tables),
+                                           tables.shape[1], _ptr(lens), B, hq, float(scale), int(window), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_paged_attention_int8 rejected its inputs")
+    return out

@@ -247,3 +247,208 @@ int oracle_paged_attention(const uint16_t *q, int64_t q_row_stride,
     }
     return failed ? -1 : 0;
 }
+
+/*
+ * ---- int8 KV cache ---------------------------------------------------------
+ *
+ * "Building a paged inference engine from scratch, and measuring it honestly",
+ * section 02 ("INT8 KV cache design"): symmetric int8, one scale per block
+ * per KV head, no zero point; on a write the block's existing entries are
+ * dequantised with the stored scale, the new entries are added, a new max-abs
+ * scale is computed over all of them and everything is requantised.  The page
+ * calls this path unverified; this is the plain reading, applied once per
+ * call to each block the call writes:
+ *
+ *   existing rows = rows 0 .. min_off-1 of the block (min_off = the lowest
+ *                   offset written into it by this call; rows are appended in
+ *                   order, so the rows below are the block's earlier tokens)
+ *   new rows      = the rows this call writes (a later token with the same slot
+ *                   replaces an earlier one)
+ *   scale         = max |x| / 127 over existing (dequantised) and new values,
+ *                   per KV head; 0 when that max is 0
+ *   code          = clamp(round_half_even(x / scale), -127, 127), 0 if scale 0
+ *
+ * Every decision that yields an integer is taken in binary32 (the kernel's
+ * precision): x as float, dequantised values q * scale as a float product,
+ * the max in float, scale = max / 127 and x / scale as IEEE float divisions,
+ * rintf for the rounding.  Rows past the highest written offset are left
+ * untouched.
+ */
+static float f32_of(uint16_t x, int dtype) { return (float)decode(x, dtype); }
+
+static int8_t quantize_f32(float x, float scale)
+{
+    if (scale == 0.0f)
+        return 0;
+    float r = rintf(x / scale);
+    if (r > 127.0f)
+        r = 127.0f;
+    if (r < -127.0f)
+        r = -127.0f;
+    return (int8_t)r;
+}
+
+/* Quantised slot write.  k/v: [T, Hkv, D] 16-bit of `dtype`; pools int8
+ * [nb, bs, Hkv, D]; scales float [nb, Hkv].  Returns 0, or -1 on a slot outside
+ * the pool (nothing written). */
+int oracle_write_kv_int8(const uint16_t *k, const uint16_t *v, int dtype, int64_t num_tokens,
+                         int num_kv_heads, int head_dim, const int64_t *slots,
+                         int8_t *kq, int8_t *vq, float *kscale, float *vscale,
+                         int64_t num_blocks, int block_size)
+{
+    const int64_t nslots = num_blocks * block_size;
+    for (int64_t t = 0; t < num_tokens; ++t)
+        if (slots[t] >= nslots)
+            return -1;
+    const int H = num_kv_heads, D = head_dim, bs = block_size;
+    /* blocks touched, in first-touch order */
+    int64_t *blocks = (int64_t *)malloc(sizeof(int64_t) * (size_t)(num_tokens > 0 ? num_tokens : 1));
+    int64_t nblk = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        if (slots[t] < 0)
+            continue;
+        int64_t b = slots[t] / bs, seen = 0;
+        for (int64_t i = 0; i < nblk; ++i)
+            if (blocks[i] == b)
+                seen = 1;
+        if (!seen)
+            blocks[nblk++] = b;
+    }
+    float *rows = (float *)malloc(sizeof(float) * (size_t)bs * D);
+    int64_t *src = (int64_t *)malloc(sizeof(int64_t) * (size_t)bs);
+    for (int which = 0; which < 2; ++which) {
+        const uint16_t *x = which ? v : k;
+        int8_t *pool = which ? vq : kq;
+        float *sc = which ? vscale : kscale;
+        for (int64_t bi = 0; bi < nblk; ++bi) {
+            const int64_t b = blocks[bi];
+            int min_off = bs, max_off = -1;
+            for (int o = 0; o < bs; ++o)
+                src[o] = -1;
+            for (int64_t t = 0; t < num_tokens; ++t) {
+                if (slots[t] < 0 || slots[t] / bs != b)
+                    continue;
+                int o = (int)(slots[t] % bs);
+                src[o] = t; /* last writer of an offset wins */
+                if (o < min_off)
+                    min_off = o;
+                if (o > max_off)
+                    max_off = o;
+            }
+            for (int h = 0; h < H; ++h) {
+                const float old = sc[b * H + h];
+                float amax = 0.0f;
+                for (int o = 0; o <= max_off; ++o) {
+                    for (int d = 0; d < D; ++d) {
+                        float val;
+                        if (src[o] >= 0)
+                            val = f32_of(x[(src[o] * H + h) * D + d], dtype);
+                        else if (o < min_off)
+                            val = (float)pool[((b * bs + o) * H + h) * D + d] * old;
+                        else
+                            val = 0.0f; /* a gap below max_off (not produced by appends) */
+                        rows[o * D + d] = val;
+                        float a = fabsf(val);
+                        if (a > amax)
+                            amax = a;
+                    }
+                }
+                const float scale = amax / 127.0f;
+                for (int o = 0; o <= max_off; ++o)
+                    for (int d = 0; d < D; ++d)
+                        pool[((b * bs + o) * H + h) * D + d] = quantize_f32(rows[o * D + d], scale);
+                sc[b * H + h] = scale;
+            }
+        }
+    }
+    free(blocks);
+    free(rows);
+    free(src);
+    return 0;
+}
+
+/* Paged attention over an int8 cache: K = code * k_scale[block][head] (exact in
+ * binary64), then the definition of oracle_paged_attention (decode rows only,
+ * optional window).  q is 16-bit of `dtype`. */
+int oracle_paged_attention_int8(const uint16_t *q, int64_t q_row_stride, int dtype,
+                                const int8_t *kq, const int8_t *vq, const float *kscale,
+                                const float *vscale, int64_t num_blocks, int block_size,
+                                int num_kv_heads, int head_dim, const int32_t *tables, int max_blocks,
+                                const int32_t *kv_lens, int num_seqs, int num_q_heads, double scale,
+                                int window, double *out)
+{
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+        return -1;
+    const int group = num_q_heads / num_kv_heads;
+    const int D = head_dim, H = num_kv_heads;
+    for (int s = 0; s < num_seqs; ++s) {
+        int64_t L = kv_lens[s];
+        if (L < 0 || L > (int64_t)max_blocks * block_size)
+            return -1;
+        for (int64_t t = 0; t < L; t += block_size) {
+            int32_t phys = tables[(int64_t)s * max_blocks + t / block_size];
+            if (phys < 0 || phys >= num_blocks)
+                return -1;
+        }
+    }
+    int failed = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int s = 0; s < num_seqs; ++s) {
+        for (int g = 0; g < H; ++g) {
+            const int64_t L = kv_lens[s];
+            const int64_t first = (window > 0 && L - window > 0) ? L - window : 0;
+            const int64_t n = L - first;
+            double *K = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * D);
+            double *V = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * D);
+            double *p = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+            double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+            if (!K || !V || !p || !qd) {
+#pragma omp atomic write
+                failed = 1;
+                free(K); free(V); free(p); free(qd);
+                continue;
+            }
+            for (int64_t i = 0; i < n; ++i) {
+                const int64_t t = first + i;
+                const int64_t phys = tables[(int64_t)s * max_blocks + t / block_size];
+                const int64_t off = t % block_size;
+                const int64_t base = ((phys * block_size + off) * H + g) * D;
+                const double sk = kscale[phys * H + g], sv = vscale[phys * H + g];
+                for (int d = 0; d < D; ++d) {
+                    K[i * D + d] = (double)kq[base + d] * sk;
+                    V[i * D + d] = (double)vq[base + d] * sv;
+                }
+            }
+            for (int h = g * group; h < (g + 1) * group; ++h) {
+                double *o = out + ((int64_t)s * num_q_heads + h) * D;
+                for (int d = 0; d < D; ++d)
+                    o[d] = 0.0;
+                if (n <= 0)
+                    continue;
+                for (int d = 0; d < D; ++d)
+                    qd[d] = decode(q[(int64_t)s * q_row_stride + (int64_t)h * D + d], dtype);
+                double mx = -INFINITY;
+                for (int64_t i = 0; i < n; ++i) {
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        dot += qd[d] * K[i * D + d];
+                    p[i] = scale * dot;
+                    if (p[i] > mx)
+                        mx = p[i];
+                }
+                double Z = 0.0;
+                for (int64_t i = 0; i < n; ++i) {
+                    p[i] = exp(p[i] - mx);
+                    Z += p[i];
+                }
+                for (int64_t i = 0; i < n; ++i)
+                    for (int d = 0; d < D; ++d)
+                        o[d] += p[i] * V[i * D + d];
+                for (int d = 0; d < D; ++d)
+                    o[d] /= Z;
+            }
+            free(K); free(V); free(p); free(qd);
+        }
+    }
+    return failed ? -1 : 0;
+}
