@@ -242,6 +242,62 @@ PKV_API pkv_status pkv_attn_varlen_window(const void *q, int64_t q_token_stride,
                                           void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
                                           int32_t *err_word, pkv_stream stream);
 
+/* ---- int8 KV cache --------------------------------------------------------- */
+/*
+ * [P4] section 02, "INT8 KV cache design": keys and values stored as
+ * symmetric int8 with one scale per block per KV head and no zero point; a
+ * write re-quantises the block (its earlier rows are dequantised with the
+ * stored scale, the new rows join them, the scale becomes max|x| / 127 and
+ * every row is re-quantised); the attention kernel dequantises right before
+ * its matrix products.  Halves the bytes a decode step reads.
+ *
+ *   k, v         int8 pools [num_blocks, block_size, num_kv_heads, head_dim]
+ *   k_scale,     float32 [num_blocks, num_kv_heads]: value = code * scale
+ *   v_scale
+ *   dtype        PKV_F16 or PKV_BF16: the type of q, of the new K/V rows given
+ *                to pkv_write_kv_int8 and of 16-bit outputs
+ * Supported on the GPU: head_dim 128, num_kv_heads a multiple of 4, the other
+ * limits of the 16-bit cache.
+ */
+typedef struct pkv_cache_i8 {
+    int8_t *k;
+    int8_t *v;
+    float *k_scale;
+    float *v_scale;
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t dtype;
+} pkv_cache_i8;
+
+/*
+ * Quantised slot write: rows k[t], v[t] (16-bit of cache->dtype, layout as in
+ * pkv_write_kv) go to slot_mapping[t].  Per block written and per KV head the
+ * block is re-quantised as above, all integer decisions in binary32 (round
+ * half to even, codes clamped to +-127, scale 0 for an all-zero block).  The
+ * block's earlier rows are those below the lowest offset the call writes into
+ * it.  The slots a call writes into one block must be consecutive entries of
+ * slot_mapping (the allocator's order); a later entry with the same slot
+ * replaces an earlier one.
+ */
+PKV_API pkv_status pkv_write_kv_int8(const void *k, const void *v, int64_t kv_token_stride,
+                                     const int64_t *slot_mapping, int32_t num_tokens, const pkv_cache_i8 *cache,
+                                     int32_t *err_word, pkv_stream stream);
+/*
+ * Decode attention over an int8 cache (arguments and errors as
+ * pkv_attn_decode_window, window <= 0 meaning none): scores use
+ * k_scale[block][head] * (q . codes), the softmax weights are multiplied by
+ * v_scale[block][head] before the product with the V codes.  Workspace size:
+ * pkv_attn_decode_workspace_size.
+ */
+PKV_API pkv_status pkv_attn_decode_int8(const void *q, int64_t q_token_stride, const pkv_cache_i8 *cache,
+                                        const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                                        float scale, int32_t window, void *out, int32_t out_dtype,
+                                        void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                        pkv_stream stream);
+
 /* ---- a10: block copy for copy-on-write ----------------------------------- */
 /*
  * [P1] Architecture Overview, copy-on-write: when sequences that share a

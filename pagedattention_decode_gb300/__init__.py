@@ -23,12 +23,12 @@ from typing import List, Optional, Sequence, Tuple
 import torch
 
 from ._native import (DEVERR, PKV_BF16, PKV_F16, PKV_F32, DoubleFreeError, ExhaustedError, PkvCache,
-                      PkvCounters, PkvError, check, lib, library_path)
+                      PkvCacheI8, PkvCounters, PkvError, check, lib, library_path)
 
 __all__ = [
     "write_kv", "attn_decode", "attn_varlen", "copy_blocks", "decode_workspace_size",
     "varlen_workspace_size", "check_copy_pairs", "BlockAllocator", "PkvError", "ExhaustedError",
-    "DoubleFreeError", "DEVERR", "library_path", "StepGraph",
+    "DoubleFreeError", "DEVERR", "library_path", "StepGraph", "write_kv_int8", "attn_decode_int8",
 ]
 
 _DT = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16, torch.float32: PKV_F32}
@@ -181,6 +181,59 @@ def attn_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
                                     block_tables.shape[1], _ptr(cu_seqlens_q), _ptr(seq_lens), B, total,
                                     int(max_q_len), hq, float(scale), 1 if causal else 0, _ptr(out), _DT[out.dtype],
                                     _ptr(ws), ws.numel() * ws.element_size(), _ptr(err), _stream(stream)))
+    return out
+
+
+def _cache_i8(kq: torch.Tensor, vq: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+              dtype: torch.dtype) -> PkvCacheI8:
+    for t, name in ((kq, "kq"), (vq, "vq"), (k_scale, "k_scale"), (v_scale, "v_scale")):
+        _cuda(t, name)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if kq.dtype != torch.int8 or vq.dtype != torch.int8 or kq.shape != vq.shape or kq.dim() != 4:
+        raise TypeError("int8 pools must be int8 [num_blocks, block_size, kv_heads, head_dim]")
+    nb, bs, hkv, d = kq.shape
+    if k_scale.dtype != torch.float32 or k_scale.shape != (nb, hkv) or v_scale.shape != (nb, hkv):
+        raise TypeError("scales must be float32 [num_blocks, kv_heads]")
+    if dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("the compute dtype must be float16 or bfloat16")
+    return PkvCacheI8(kq.data_ptr(), vq.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(), nb, bs, hkv, d,
+                      _DT[dtype])
+
+
+def write_kv_int8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, kq: torch.Tensor, vq: torch.Tensor,
+                  k_scale: torch.Tensor, v_scale: torch.Tensor, err: Optional[torch.Tensor] = None,
+                  stream=None) -> None:
+    """Quantised write of rows k[t], v[t] (fp16/bf16 [T, Hkv, D]) into an int8 cache; the blocks
+    written are re-quantised with a new per-block-per-head scale."""
+    c = _cache_i8(kq, vq, k_scale, v_scale, k.dtype)
+    _cuda(k, "k")
+    _cuda(v, "v")
+    _cuda(slot_mapping, "slot_mapping")
+    if slot_mapping.dtype != torch.int64 or k.shape != v.shape or k.shape[0] != slot_mapping.numel():
+        raise ValueError("k, v [T, kv_heads, head_dim] and int64 slot_mapping [T] expected")
+    check(lib().pkv_write_kv_int8(_ptr(k), _ptr(v), _row_stride(k, "k"), _ptr(slot_mapping), k.shape[0],
+                                  ctypes.byref(c), _ptr(err), _stream(stream)))
+
+
+def attn_decode_int8(q: torch.Tensor, kq: torch.Tensor, vq: torch.Tensor, k_scale: torch.Tensor,
+                     v_scale: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                     window: int = 0, out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.float32,
+                     workspace: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    """Decode attention over an int8 cache; q fp16/bf16 [B, Hq, D]."""
+    c = _cache_i8(kq, vq, k_scale, v_scale, q.dtype)
+    _cuda(q, "q")
+    _check_i32(block_tables, "block_tables")
+    _check_i32(seq_lens, "seq_lens")
+    B, hq, d = q.shape
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
+    ws = _workspace(lambda: decode_workspace_size(B, hq, c.num_kv_heads, d, q.device.index), workspace, q.device)
+    check(lib().pkv_attn_decode_int8(_ptr(q), _row_stride(q, "q"), ctypes.byref(c), _ptr(block_tables),
+                                     block_tables.shape[1], _ptr(seq_lens), B, hq, float(scale), int(window),
+                                     _ptr(out), _DT[out.dtype], _ptr(ws), ws.numel() * ws.element_size(), _ptr(err),
+                                     _stream(stream)))
     return out
 
 

@@ -42,6 +42,12 @@ class PkvCache(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
+class PkvCacheI8(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
 class PkvCounters(ctypes.Structure):
     _fields_ = [("allocs", ctypes.c_int64), ("frees", ctypes.c_int64),
                 ("cow_copies", ctypes.c_int64), ("peak_used", ctypes.c_int64)]
@@ -67,6 +73,9 @@ SIGNATURES = {
                                       _i32, _vp, _sz, _vp, _vp]),
     "pkv_attn_varlen_window": (_i32, [_vp, _i64, _P(PkvCache), _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
                                       _f32, _i32, _i32, _vp, _i32, _vp, _sz, _vp, _vp]),
+    "pkv_write_kv_int8": (_i32, [_vp, _vp, _i64, _vp, _i32, _P(PkvCacheI8), _vp, _vp]),
+    "pkv_attn_decode_int8": (_i32, [_vp, _i64, _P(PkvCacheI8), _vp, _i32, _vp, _i32, _i32, _f32, _i32, _vp, _i32,
+                                    _vp, _sz, _vp, _vp]),
     "pkv_copy_blocks": (_i32, [_P(PkvCache), _i32, _vp, _i32, _vp, _vp]),
     "pkv_check_copy_pairs": (_i32, [_vp, _i32, _i32]),
     "pkv_alloc_create": (_i32, [_i32, _i32, _P(_vp)]),

@@ -61,6 +61,8 @@ struct DecodeParams {
     int32_t *err;
     int32_t stages;
     int32_t window;                // > 0: attend only the last `window` keys
+    const float *k_scale;          // int8 cache: [num_blocks, hkv] scales (NULL for 16-bit caches)
+    const float *v_scale;
 };
 
 // First key a decode row of a sequence with L keys attends (sliding window).
@@ -111,16 +113,47 @@ __device__ __forceinline__ int block_scan(int v, int *warp_sums, int *total) {
     return x + before;
 }
 
+// Two int8 codes -> a packed 16-bit pair.  `x` holds four codes XOR 0x80
+// (offset binary); `sel` is a byte_perm selector 0x4?4? naming the bytes for
+// the low and high halves.  fp16: bytes under the exponent of 1024 give
+// 1024 + u exactly, minus 1152 = the signed code.  bf16: through binary32
+// (2^23 + u, minus 2^23 + 128), then an exact narrowing.
+template <typename T>
+__device__ __forceinline__ uint32_t i8_pair(uint32_t x, uint32_t sel);
+
+template <>
+__device__ __forceinline__ uint32_t i8_pair<__half>(uint32_t x, uint32_t sel) {
+    uint32_t h = __byte_perm(x, 0x64646464u, sel);
+    __half2 v = __hsub2(*reinterpret_cast<__half2 *>(&h), __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <>
+__device__ __forceinline__ uint32_t i8_pair<__nv_bfloat16>(uint32_t x, uint32_t sel) {
+    const float lo = __int_as_float((int)__byte_perm(x, 0x4B000000u, 0x7540u | (sel & 0xFu))) - 8388736.f;
+    const float hi = __int_as_float((int)__byte_perm(x, 0x4B000000u, 0x7540u | ((sel >> 8) & 0xFu))) - 8388736.f;
+    return pack2<__nv_bfloat16>(lo, hi);
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // The CTA that owns concatenated sub-block x when `ctas` ranges split `total`.
 __device__ __forceinline__ int range_owner(int64_t x, int64_t total, int64_t ctas) {
     return (int)(((x + 1) * ctas - 1) / total);
 }
 
-template <int D, typename T>
+template <int D, typename T, bool I8>
 __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
     decode_splitk_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                          const DecodeParams p) {
-    constexpr int HALVES = D / 64;
+    // 2 KB shared tiles per KV head per sub-block: 16 tokens x 64 dims of a
+    // 16-bit cache (two for head_dim 128), or 16 tokens x 128 int8 codes
+    constexpr int HALVES = I8 ? 1 : D / 64;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_warp[32];
     __shared__ int s_first_seq, s_first_start;
@@ -134,6 +167,7 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(base + NS * stage_bytes);
     uint64_t *empty = full + NS;
+    float *sscale = reinterpret_cast<float *>(empty + NS);  // int8: [NS][2][hkv] per-stage block scales
     const int hg = blockIdx.y;
     const bool meta_cta = blockIdx.x == 0 && blockIdx.y == 0;
 
@@ -212,7 +246,7 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
             const int sb0 = decode_first_key(p, p.seq_lens[s]) / kSub;  // window: first sub-block
             for (int j0 = sb; j0 < b1 && !aborted; j0 += 32) {
                 const int jn = min(32, b1 - j0);
-                int row = 0;
+                int row = 0, pblk = 0;
                 if (lane < jn) {
                     const int tok = (sb0 + j0 + lane) * kSub;
                     const int lb = tok / p.block_size;
@@ -221,10 +255,12 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
                         set_err(p.err, PKV_DEVERR_BLOCK);
                         phys = 0;
                     }
+                    pblk = phys;
                     row = phys * p.block_size + (tok - lb * p.block_size);
                 }
                 for (int j = 0; j < jn; ++j) {
                     const int r = __shfl_sync(0xffffffffu, row, j);
+                    const int rb = __shfl_sync(0xffffffffu, pblk, j);
                     const int stage = it % NS;
                     int okw = 1;
                     if (lane == 0) okw = mbar_wait(&empty[stage], ((it / NS) & 1) ^ 1, &s_abort);
@@ -233,8 +269,16 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
                         aborted = true;
                         break;
                     }
-                    if (lane == 0) mbar_arrive_expect_tx(&full[stage], stage_bytes);
+                    const uint32_t scale_bytes = I8 ? (uint32_t)(8 * p.hkv) : 0u;
+                    if (lane == 0) mbar_arrive_expect_tx(&full[stage], stage_bytes + scale_bytes);
                     __syncwarp();
+                    if constexpr (I8) {
+                        if (lane == 0) {
+                            float *ds = sscale + stage * 2 * p.hkv;
+                            bulk_copy_g2s(ds, p.k_scale + (int64_t)rb * p.hkv, 4 * p.hkv, &full[stage]);
+                            bulk_copy_g2s(ds + p.hkv, p.v_scale + (int64_t)rb * p.hkv, 4 * p.hkv, &full[stage]);
+                        }
+                    }
                     uint8_t *sbase = base + stage * stage_bytes;
                     for (int tt = lane; tt < 2 * tiles; tt += 32) {
                         const int which = tt >= tiles;
@@ -301,8 +345,9 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 if (g < G) {
-                    qf[kk][0] = *reinterpret_cast<const uint32_t *>(qp + kk * 16 + 2 * t4);
-                    qf[kk][1] = *reinterpret_cast<const uint32_t *>(qp + kk * 16 + 8 + 2 * t4);
+                    // int8: dims permuted inside each 16-dim step to match the K codes' byte order
+                    qf[kk][0] = *reinterpret_cast<const uint32_t *>(qp + kk * 16 + (I8 ? 4 * t4 : 2 * t4));
+                    qf[kk][1] = *reinterpret_cast<const uint32_t *>(qp + kk * 16 + (I8 ? 4 * t4 + 2 : 8 + 2 * t4));
                 } else {
                     qf[kk][0] = 0u;
                     qf[kk][1] = 0u;
@@ -329,7 +374,27 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
 
             // S^T[16 tokens x 8 heads] = K q^T
             float sc[4] = {0.f, 0.f, 0.f, 0.f};
-            {
+            float ssl = sl, vsc = 1.f;
+            if constexpr (I8) {
+                const float *st_scale = sscale + stage * 2 * p.hkv;
+                ssl = sl * st_scale[kvh];
+                vsc = st_scale[p.hkv + kvh];
+                // codes of 16 tokens x 32 dims per ldmatrix.x4; thread t of a row holds dims 4t..4t+3
+                const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                for (int k2 = 0; k2 < D / 32; ++k2) {
+                    const int chunk = 2 * k2 + (lane >> 4);
+                    uint32_t r[4];
+                    ldmatrix_x4(r, smem_u32(kb + tok * 128 + ((chunk ^ (tok & 7)) << 4)));
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t lo = r[2 * u] ^ 0x80808080u, hi = r[2 * u + 1] ^ 0x80808080u;
+                        const uint32_t a[4] = {i8_pair<T>(lo, 0x4140u), i8_pair<T>(hi, 0x4140u),
+                                               i8_pair<T>(lo, 0x4342u), i8_pair<T>(hi, 0x4342u)};
+                        mma_16816<T>(sc, a, qf[2 * k2 + u][0], qf[2 * k2 + u][1]);
+                    }
+                }
+            } else {
                 const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -339,7 +404,7 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
                     mma_16816<T>(sc, a, qf[kk][0], qf[kk][1]);
                 }
             }
-            float x0 = sc[0] * sl, x1 = sc[1] * sl, x2 = sc[2] * sl, x3 = sc[3] * sl;
+            float x0 = sc[0] * ssl, x1 = sc[1] * ssl, x2 = sc[2] * ssl, x3 = sc[3] * ssl;
             if (nv < kSub) {
                 if (g >= nv) x0 = x1 = -INFINITY;
                 if (g + 8 >= nv) x2 = x3 = -INFINITY;
@@ -372,9 +437,11 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
                 o[mt][3] *= aB;
             }
             // P as the B operand (16 tokens x 8 heads), hi and lo 16-bit parts
-            const uint32_t h01 = pack2<T>(p0, p1), h23 = pack2<T>(p2, p3);
+            // (int8: P is scaled by the block's V scale, so the codes multiply directly)
+            const float q0 = p0 * vsc, q1 = p1 * vsc, q2 = p2 * vsc, q3 = p3 * vsc;
+            const uint32_t h01 = pack2<T>(q0, q1), h23 = pack2<T>(q2, q3);
             const float2 r01 = unpack2<T>(h01), r23 = unpack2<T>(h23);
-            const uint32_t l01 = pack2<T>(p0 - r01.x, p1 - r01.y), l23 = pack2<T>(p2 - r23.x, p3 - r23.y);
+            const uint32_t l01 = pack2<T>(q0 - r01.x, q1 - r01.y), l23 = pack2<T>(q2 - r23.x, q3 - r23.y);
             const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
             const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
             uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
@@ -383,7 +450,25 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
                 m23 = (2 * t4 + 8 < nv ? 0x0000ffffu : 0u) | (2 * t4 + 9 < nv ? 0xffff0000u : 0u);
             }
             // O^T[16 dims x 8 heads] += V^T P
-            {
+            if constexpr (I8) {
+                // codes of 16 tokens x 32 dims per ldmatrix.x4.trans; M row g of an
+                // m tile is dim 2g, row g + 8 is dim 2g + 1 (see the output mapping)
+                const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                for (int m2 = 0; m2 < D / 32; ++m2) {
+                    const int chunk = 2 * m2 + (lane >> 4);
+                    uint32_t r[4];
+                    ldmatrix_x4_trans(r, smem_u32(vb + tok * 128 + ((chunk ^ (tok & 7)) << 4)));
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t lo = r[2 * u] ^ 0x80808080u, hi = r[2 * u + 1] ^ 0x80808080u;
+                        const uint32_t a[4] = {i8_pair<T>(lo, 0x4240u), i8_pair<T>(lo, 0x4341u),
+                                               i8_pair<T>(hi, 0x4240u), i8_pair<T>(hi, 0x4341u)};
+                        mma_16816<T>(o[2 * m2 + u], a, bh0, bh1);
+                        mma_16816<T>(o[2 * m2 + u], a, bl0, bl1);
+                    }
+                }
+            } else {
                 const int tok = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
@@ -420,7 +505,7 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
             const int64_t ob = (qrow * (int64_t)(p.hkv * G) + (int64_t)kvh * G) * D;
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
-                const int d0 = mt * 16 + g, d1 = d0 + 8;
+                const int d0 = I8 ? mt * 16 + 2 * g : mt * 16 + g, d1 = I8 ? d0 + 1 : d0 + 8;
                 if (p.out_f32) {
                     float *op = static_cast<float *>(p.out) + ob;
                     if (hA < G) {
@@ -450,7 +535,7 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
             float *wml = p.ws_ml + rec * 2;
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
-                const int d0 = mt * 16 + g, d1 = d0 + 8;
+                const int d0 = I8 ? mt * 16 + 2 * g : mt * 16 + g, d1 = I8 ? d0 + 1 : d0 + 8;
                 if (hA < G) {
                     wo[hA * D + d0] = o[mt][0];
                     wo[hA * D + d1] = o[mt][2];
@@ -613,8 +698,8 @@ struct DecodePlan {
     size_t meta_bytes, ml_bytes, o_bytes;
 };
 
-static int pick_heads_per_cta(int hkv, int head_dim) {
-    const int halves = head_dim / 64;
+static int pick_heads_per_cta(int hkv, int head_dim, bool i8) {
+    const int halves = i8 ? 1 : head_dim / 64;  // 2 KB tiles per head per K (or V)
     const int cap = head_dim == 64 ? max_heads_per_cta<64>() : max_heads_per_cta<128>();
     for (int hg = cap < hkv ? cap : hkv; hg >= 1; --hg)
         if (hkv % hg == 0 && hg * halves * 2 * kTile <= 64 * 1024) return hg;
@@ -624,19 +709,20 @@ static int pick_heads_per_cta(int hkv, int head_dim) {
 static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static pkv_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, int32_t head_dim, int32_t device,
-                            DecodePlan *pl) {
+                            DecodePlan *pl, bool i8 = false) {
     int sms = 0;
     pkv_status st = sm_count(device, &sms);
     if (st != PKV_OK) return st;
-    pl->heads_per_cta = pick_heads_per_cta(hkv, head_dim);
+    pl->heads_per_cta = pick_heads_per_cta(hkv, head_dim, i8);
     pl->num_hg = hkv / pl->heads_per_cta;
     // persistent: all CTAs (one per SM over all head groups) resident at once
     pl->cmax = sms / pl->num_hg > 0 ? sms / pl->num_hg : 1;
-    const int stage_bytes = pl->heads_per_cta * (head_dim / 64) * 2 * kTile;
+    const int stage_bytes = pl->heads_per_cta * (i8 ? 1 : head_dim / 64) * 2 * kTile;
     int ns = (200 * 1024) / stage_bytes;
     pl->stages = ns > 16 ? 16 : (ns < 2 ? 2 : ns);
     pl->threads = 32 * (1 + pl->heads_per_cta);
-    pl->smem_bytes = pl->stages * stage_bytes + 1024 + 2 * pl->stages * 8;  // <= 210 KB (set once per device)
+    // stages, alignment slack, barriers, and (int8) two scale rows per stage; <= 210 KB (set once per device)
+    pl->smem_bytes = pl->stages * stage_bytes + 1024 + 2 * pl->stages * 8 + (i8 ? pl->stages * 8 * hkv : 0);
     const int group = num_q_heads / hkv;
     const size_t recs = (size_t)pl->num_hg * pl->cmax * 2 * pl->heads_per_cta * group;
     pl->meta_bytes = round256(sizeof(int32_t) * (size_t)(num_seqs + 3));
@@ -645,10 +731,10 @@ static pkv_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, 
     return PKV_OK;
 }
 
-template <int D, typename T>
+template <int D, typename T, bool I8 = false>
 static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
                                   const DecodePlan &pl, cudaStream_t stream) {
-    auto kern = decode_splitk_kernel<D, T>;
+    auto kern = decode_splitk_kernel<D, T, I8>;
     // the plan's shared memory depends only on (D, heads per CTA); size for the largest plan once
     static std::atomic<uint64_t> smem_set{0};
     pkv_status st = set_smem_once(reinterpret_cast<const void *>(kern), 210 * 1024, &smem_set);
@@ -736,6 +822,55 @@ pkv_status run_decode(const void *q, int64_t q_stride, const pkv_cache *cache, c
                              out, out_dtype, workspace, workspace_bytes, err_word, stream);
 }
 
+pkv_status check_cache_i8(const pkv_cache_i8 *c, const char *what);  // int8_write.cu
+
+static pkv_status run_decode_i8(const void *q, int64_t q_stride, const pkv_cache_i8 *cache, const int32_t *tables,
+                                int32_t max_blocks, const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                                float scale, int32_t window, void *out, int32_t out_dtype, void *workspace,
+                                size_t workspace_bytes, int32_t *err_word, cudaStream_t stream) {
+    DecodePlan pl;
+    pkv_status st = make_plan(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, -1, &pl, true);
+    if (st != PKV_OK) return st;
+    const size_t need = pl.meta_bytes + pl.ml_bytes + pl.o_bytes;
+    PKV_CHECK_ARG(workspace && workspace_bytes >= need, PKV_ERR_WORKSPACE,
+                  "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+    PKV_CHECK_ARG((reinterpret_cast<uintptr_t>(workspace) & 255) == 0, PKV_ERR_INVALID_ARG,
+                  "workspace must be 256-byte aligned");
+    CUtensorMap mk, mv;
+    st = encode_pool_map_i8(&mk, cache->k, cache);
+    if (st != PKV_OK) return st;
+    st = encode_pool_map_i8(&mv, cache->v, cache);
+    if (st != PKV_OK) return st;
+    DecodeParams p{};
+    p.q = q;
+    p.q_stride = q_stride;
+    p.tables = tables;
+    p.max_blocks = max_blocks;
+    p.seq_lens = seq_lens;
+    p.cu_q = nullptr;
+    p.num_seqs = num_seqs;
+    p.num_blocks = cache->num_blocks;
+    p.block_size = cache->block_size;
+    p.hkv = cache->num_kv_heads;
+    p.heads_per_cta = pl.heads_per_cta;
+    p.group = num_q_heads / cache->num_kv_heads;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out = out;
+    p.out_f32 = out_dtype == PKV_F32;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    p.ws_meta = reinterpret_cast<int32_t *>(ws);
+    p.ws_ml = reinterpret_cast<float *>(ws + pl.meta_bytes);
+    p.ws_o = reinterpret_cast<float *>(ws + pl.meta_bytes + pl.ml_bytes);
+    p.cmax = pl.cmax;
+    p.err = err_word;
+    p.stages = pl.stages;
+    p.window = window > 0 ? window : 0;
+    p.k_scale = cache->k_scale;
+    p.v_scale = cache->v_scale;
+    return cache->dtype == PKV_BF16 ? launch_decode_t<128, __nv_bfloat16, true>(mk, mv, p, pl, stream)
+                                    : launch_decode_t<128, __half, true>(mk, mv, p, pl, stream);
+}
+
 pkv_status decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, int32_t head_dim,
                                  int32_t device, size_t *bytes) {
     DecodePlan pl;
@@ -803,6 +938,34 @@ pkv_status pkv_attn_decode_window(const void *q, int64_t q_token_stride, const p
     if (num_seqs == 0) return ok();
     st = run_decode_window(q, q_token_stride, cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
                            num_q_heads, scale, window, out, out_dtype, workspace, workspace_bytes, err_word, stream);
+    return st == PKV_OK ? ok() : st;
+}
+
+pkv_status pkv_attn_decode_int8(const void *q, int64_t q_token_stride, const pkv_cache_i8 *cache,
+                                const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                int32_t num_seqs, int32_t num_q_heads, float scale, int32_t window, void *out,
+                                int32_t out_dtype, void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                pkv_stream stream) {
+    pkv_status st = check_cache_i8(cache, "pkv_attn_decode_int8");
+    if (st != PKV_OK) return st;
+    PKV_CHECK_ARG(cache->head_dim == 128, PKV_ERR_UNSUPPORTED, "int8 decode: head_dim must be 128");
+    PKV_CHECK_ARG(cache->num_kv_heads % 4 == 0, PKV_ERR_UNSUPPORTED, "int8 decode: num_kv_heads must be a multiple of 4");
+    PKV_CHECK_ARG(cache->block_size % 16 == 0, PKV_ERR_UNSUPPORTED, "int8 decode: block_size must be a multiple of 16");
+    PKV_CHECK_ARG(num_q_heads > 0 && num_q_heads % cache->num_kv_heads == 0, PKV_ERR_SHAPE,
+                  "num_q_heads must be a multiple of num_kv_heads");
+    const int group = num_q_heads / cache->num_kv_heads;
+    PKV_CHECK_ARG(group == 1 || group == 2 || group == 4 || group == 8, PKV_ERR_UNSUPPORTED,
+                  "query heads per KV head must be 1, 2, 4 or 8");
+    PKV_CHECK_ARG(num_seqs >= 0 && max_blocks_per_seq >= 0, PKV_ERR_INVALID_ARG, "negative size");
+    PKV_CHECK_ARG(out_dtype == PKV_F32 || out_dtype == cache->dtype, PKV_ERR_DTYPE, "out dtype must be F32 or q's");
+    PKV_CHECK_ARG(q_token_stride >= (int64_t)num_q_heads * 128 && q_token_stride % 2 == 0 &&
+                      (reinterpret_cast<uintptr_t>(q) & 7) == 0,
+                  PKV_ERR_INVALID_ARG, "q rows must be 8-byte aligned and at least one row long");
+    PKV_CHECK_ARG(aligned16(out), PKV_ERR_INVALID_ARG, "out must be 16-byte aligned");
+    if (num_seqs == 0) return ok();
+    PKV_CHECK_ARG(q && block_tables && seq_lens && out, PKV_ERR_INVALID_ARG, "NULL pointer");
+    st = run_decode_i8(q, q_token_stride, cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_q_heads,
+                       scale, window, out, out_dtype, workspace, workspace_bytes, err_word, stream);
     return st == PKV_OK ? ok() : st;
 }
 

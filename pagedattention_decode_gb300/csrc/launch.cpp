@@ -91,6 +91,20 @@ pkv_status encode_pool_map(CUtensorMap *map, void *base, const pkv_cache *c) {
     return PKV_OK;
 }
 
+pkv_status encode_pool_map_i8(CUtensorMap *map, void *base, const pkv_cache_i8 *c) {
+    auto fn = encode_fn();
+    PKV_CHECK_ARG(fn, PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_kv_heads,
+                          (cuuint64_t)c->num_blocks * c->block_size};
+    cuuint64_t strides[2] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_kv_heads * c->head_dim};
+    cuuint32_t box[3] = {128, 1, 16};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    PKV_CHECK_ARG(r == CUDA_SUCCESS, PKV_ERR_CUDA, "cuTensorMapEncodeTiled (int8 pool) failed (%d)", (int)r);
+    return PKV_OK;
+}
+
 pkv_status encode_q_map(CUtensorMap *map, const void *q, int64_t q_stride, int total_q, int hq, int d, int rows,
                         int dtype) {
     auto fn = encode_fn();

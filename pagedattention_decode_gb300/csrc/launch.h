@@ -38,6 +38,10 @@ pkv_status set_smem_once(const void *kernel, int bytes, std::atomic<uint64_t> *d
 // = 16 rows x 1 tile x 64 elements, 128-byte swizzle (a 2 KB shared tile).
 pkv_status encode_pool_map(CUtensorMap *map, void *base, const pkv_cache *c);
 
+// The same for an int8 pool with head_dim 128: box = 16 rows x 1 head x 128
+// codes (one 2 KB shared tile per KV head per 16 tokens).
+pkv_status encode_pool_map_i8(CUtensorMap *map, void *base, const pkv_cache_i8 *c);
+
 // 3-D tensor map over packed query rows [total_q][Hq * D / 64][64] (row
 // stride q_stride elements), box = `rows` rows x 1 x 64 elements, 128-byte
 // swizzle: one head-half of `rows` consecutive query rows per load.

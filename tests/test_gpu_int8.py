@@ -1,0 +1,92 @@
+"""int8 KV cache on the GPU: quantised writes bit-exact against the oracle's
+writer, int8 decode attention within 2e-3 of the binary64 int8 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pagedattention_decode_gb300 as P
+import workloads as W
+from oracle.allocator import RefAllocator
+from tests.cases import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _pools(nb, bs, hkv, d):
+    return (np.zeros((nb, bs, hkv, d), np.int8), np.zeros((nb, bs, hkv, d), np.int8),
+            np.zeros((nb, hkv), np.float32), np.zeros((nb, hkv), np.float32))
+
+
+def _dev(*arrs):
+    return [torch.from_numpy(a.copy()).cuda() for a in arrs]
+
+
+@pytest.mark.parametrize("dtype,bs", [("f16", 16), ("bf16", 32), ("f16", 64)])
+def test_int8_write_bit_exact(dtype, bs):
+    nb, hkv, d = 48, 8, 128
+    g = W.generator(500 + bs)
+    a = RefAllocator(nb, bs)
+    a.set_free_order(W.permutation(g, nb))
+    kq, vq, ks, vs = _pools(nb, bs, hkv, d)
+    dk, dv, dks, dvs = _dev(kq, vq, ks, vs)
+    seqs = [a.create_sequence() for _ in range(5)]
+    # prefill runs, then several decode steps (each re-quantises the tail block)
+    for counts in ([37, 1, bs, 2 * bs + 3, 5], [1] * 5, [1] * 5, [3, 1, 0, 1, bs + 1], [1] * 5):
+        slots, _ = a.append_tokens(seqs, counts)
+        T = len(slots)
+        k = W.normal(g, (T, hkv, d), 1.0 + 0.1 * T % 3, dtype)
+        v = W.normal(g, (T, hkv, d), 0.7, dtype)
+        oracle.write_kv_int8(k, v, dtype, slots, kq, vq, ks, vs)
+        P.write_kv_int8(k.cuda(), v.cuda(), torch.tensor(slots, dtype=torch.int64, device="cuda"), dk, dv, dks, dvs)
+        torch.cuda.synchronize()
+        assert np.array_equal(dk.cpu().numpy(), kq) and np.array_equal(dv.cpu().numpy(), vq)
+        assert np.array_equal(dks.cpu().numpy(), ks) and np.array_equal(dvs.cpu().numpy(), vs)
+
+
+def _int8_case(seed, lens, hq, hkv, bs, dtype, nb=None):
+    d = 128
+    g = W.generator(seed)
+    need = sum(W.blocks_for(L, bs) for L in lens)
+    nb = nb or need + 8
+    a = RefAllocator(nb, bs)
+    a.set_free_order(W.permutation(g, nb))
+    kq, vq, ks, vs = _pools(nb, bs, hkv, d)
+    seqs = [a.create_sequence() for _ in lens]
+    slots, _ = a.append_tokens(seqs, lens)
+    k = W.normal(g, (len(slots), hkv, d), 1.0, dtype)
+    v = W.normal(g, (len(slots), hkv, d), 1.0, dtype)
+    oracle.write_kv_int8(k, v, dtype, slots, kq, vq, ks, vs)
+    mb = max(W.blocks_for(L, bs) for L in lens) + 1
+    tables = np.full((len(lens), mb), -1, np.int32)
+    for i, s in enumerate(seqs):
+        t = a.block_table(s)
+        tables[i, :len(t)] = t
+    q = W.normal(g, (len(lens), hq, d), 1.0, dtype)
+    return q, kq, vq, ks, vs, tables, np.array(lens, np.int32)
+
+
+@pytest.mark.parametrize("hq,hkv,bs,dtype", [(32, 8, 16, "f16"), (32, 8, 32, "bf16"), (32, 4, 16, "f16"),
+                                             (8, 8, 16, "bf16")])
+@pytest.mark.parametrize("window", [0, 100])
+def test_int8_decode_matches_oracle(hq, hkv, bs, dtype, window):
+    lens = [1, 15, 16, 17, 33, 300, 1000, 2500] + [0]
+    q, kq, vq, ks, vs, tables, L = _int8_case(600 + hq + bs, lens, hq, hkv, bs, dtype)
+    scale = 128 ** -0.5
+    dk, dv, dks, dvs = _dev(kq, vq, ks, vs)
+    out = P.attn_decode_int8(q.cuda(), dk, dv, dks, dvs, torch.from_numpy(tables).cuda(),
+                             torch.from_numpy(L).cuda(), scale, window=window)
+    torch.cuda.synchronize()
+    want = oracle.paged_attention_int8(q, dtype, kq, vq, ks, vs, tables, L, scale, window=window)
+    assert_close(out, want, what=f"int8 {hq}/{hkv}/{bs}/{dtype}/w{window}")
+
+
+def test_int8_decode_long_split_and_16bit_out():
+    lens = [30000, 5, 4000]
+    q, kq, vq, ks, vs, tables, L = _int8_case(700, lens, 32, 8, 16, "f16")
+    dk, dv, dks, dvs = _dev(kq, vq, ks, vs)
+    out = P.attn_decode_int8(q.cuda(), dk, dv, dks, dvs, torch.from_numpy(tables).cuda(), torch.from_numpy(L).cuda(),
+                             0.088, out_dtype=torch.float16)
+    torch.cuda.synchronize()
+    want = oracle.paged_attention_int8(q, "f16", kq, vq, ks, vs, tables, L, 0.088)
+    assert_close(out, want, what="int8 long")
