@@ -251,6 +251,44 @@ class DecodeStep:
         return dec, write_bytes(w.batch, w.num_kv_heads, w.head_dim, 2)
 
 
+class DecodeStepInt8(DecodeStep):
+    """The same decode step over an int8 cache (codes and per-block-per-head
+    scales): write = quantised write of the new rows (re-quantising their
+    blocks), decode = int8 split-K decode."""
+
+    def __init__(self, w: W.Workload, dev: torch.device):
+        super().__init__(w, dev)
+        B, hkv, d, bs = w.batch, w.num_kv_heads, w.head_dim, w.block_size
+        g = torch.Generator(device=str(dev))
+        g.manual_seed(w.seed * 100 + 77)
+        shape = (w.num_blocks, bs, hkv, d)
+        self.kq = [torch.randint(-127, 128, shape, generator=g, dtype=torch.int8, device=dev) for _ in range(w.layers)]
+        self.vq = [torch.randint(-127, 128, shape, generator=g, dtype=torch.int8, device=dev) for _ in range(w.layers)]
+        self.ks = [torch.rand((w.num_blocks, hkv), generator=g, device=dev) * 0.03 + 0.01 for _ in range(w.layers)]
+        self.vs = [torch.rand((w.num_blocks, hkv), generator=g, device=dev) * 0.03 + 0.01 for _ in range(w.layers)]
+        self.k_caches = self.v_caches = None  # the 16-bit pools are not used
+        torch.cuda.empty_cache()
+
+    def write(self, layer=0):
+        self.P.write_kv_int8(self.k_new, self.v_new, self.slots, self.kq[layer], self.vq[layer], self.ks[layer],
+                             self.vs[layer], err=self.err)
+
+    def decode(self, layer=0):
+        self.P.attn_decode_int8(self.q, self.kq[layer], self.vq[layer], self.ks[layer], self.vs[layer], self.tables,
+                                self.lens, self.w.scale, out=self.out, workspace=self.ws, err=self.err)
+
+    def bytes(self):
+        w = self.w
+        hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
+        dec = decode_bytes(w.lengths, hq, hkv, d, 1, 4, self.sms, self.num_hg)
+        dec += len(w.lengths) * hq * d * 1  # q is 16-bit (decode_bytes counted it at 1 byte)
+        dec += sum(-(-L // 16) for L in w.lengths) * 2 * hkv * 4  # the scale rows read per sub-block
+        # each new token re-quantises its block: earlier rows read and rewritten, K and V
+        wr = sum(2 * ((L - 1) % w.block_size) * hkv * d * 2 + 2 * hkv * d * (2 + 1) + 16 * hkv
+                 for L in w.lengths)
+        return dec, wr
+
+
 def time_device(step: DecodeStep, steps: int, warmup: int, barrier):
     stream = torch.cuda.current_stream()
     layers = step.w.layers
@@ -639,8 +677,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                     help="replay each timed step as one CUDA graph (auto: on for multi-layer workloads)")
-    ap.add_argument("--workload", default="gqa", choices=["gqa", "gpt2", "skew", "mixed"],
-                    help="gqa: the headline decode step (GQA 32/8, B 256); gpt2: 12-layer MHA decode step; "
+    ap.add_argument("--workload", default="gqa", choices=["gqa", "gqa_int8", "gpt2", "skew", "mixed"],
+                    help="gqa: the headline decode step (GQA 32/8, B 256); gqa_int8: the same over an int8 "
+                         "cache; gpt2: 12-layer MHA decode step; "
                          "skew: long/skewed split-K decode; mixed: the packed prefill+decode step")
     ap.add_argument("--batch", type=int, default=0,
                     help="use only the first N sequences (a smaller case of the same workload, for profiling)")
@@ -674,10 +713,11 @@ def main():
     assert args.warmup >= 3, "at least 3 warm-up steps"
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = {"gqa": W.gqa_decode, "gpt2": W.gpt2_decode, "skew": W.long_skewed_decode}[args.workload]()
+    w = {"gqa": W.gqa_decode, "gqa_int8": W.gqa_decode, "gpt2": W.gpt2_decode,
+         "skew": W.long_skewed_decode}[args.workload]()
     if args.batch:
         w = W.first_sequences(w, args.batch)
-    step = DecodeStep(w, dev)
+    step = DecodeStepInt8(w, dev) if args.workload == "gqa_int8" else DecodeStep(w, dev)
     use_graph = args.graph == "on" or (args.graph == "auto" and w.layers > 1)
     timer = time_device_graph if use_graph else time_device
     total_ms, dec_ms, wr_ms, clocks = timer(step, args.steps, args.warmup, barrier)
@@ -705,15 +745,19 @@ def main():
         "config": {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "block_size": w.block_size, "mean_context": sum(w.lengths) / w.batch,
                    "layers": w.layers,
-                   "kv_bytes_per_step": w.layers * sum(w.lengths) * kv_bytes_per_token(w.num_kv_heads, w.head_dim, 2),
-                   "dtype": w.dtype,
+                   "kv_bytes_per_step": w.layers * sum(w.lengths) * kv_bytes_per_token(
+                       w.num_kv_heads, w.head_dim, 1 if args.workload == "gqa_int8" else 2),
+                   "dtype": w.dtype, "kv_cache": "int8 + per-block-per-head fp32 scales"
+                   if args.workload == "gqa_int8" else w.dtype,
                    "l2": ("inputs larger than L2 (%.2f GB of K/V per step vs 129 MB), no flush" %
-                          (w.layers * sum(w.lengths) * kv_bytes_per_token(w.num_kv_heads, w.head_dim, 2) / 1e9)),
+                          (w.layers * sum(w.lengths) * kv_bytes_per_token(
+                              w.num_kv_heads, w.head_dim, 1 if args.workload == "gqa_int8" else 2) / 1e9)),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "tokens_per_s": tokens_per_s,
         "pct_of_hbm": {"nominal_8TBs": 100.0 * value / world / NOMINAL_HBM_GBS,
                        f"{peak_kind}_{peak:.0f}GBs": 100.0 * value / world / peak},
-        "roofline": {"bound": "hbm", "kernel": "pkv_attn_decode (split-K decode + merge)",
+        "roofline": {"bound": "hbm", "kernel": ("pkv_attn_decode_int8" if args.workload == "gqa_int8"
+                                                 else "pkv_attn_decode") + " (split-K decode + merge)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy, burst)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "traffic": traffic,
@@ -725,7 +769,7 @@ def main():
         "clocks": clocks,
         "gpu_launches": args.steps * 3 * w.layers,
     }
-    if not args.no_e2e and w.layers == 1:
+    if not args.no_e2e and w.layers == 1 and args.workload != "gqa_int8":
         e2e_ms, e2e_bytes, h2d, d2h = time_e2e(w, step, max(1, min(args.steps, 200)), 3, barrier)
         n_e2e = max(1, min(args.steps, 200))
         line["e2e"] = {"value": world * e2e_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,

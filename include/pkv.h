@@ -151,7 +151,8 @@ PKV_API pkv_status pkv_write_kv(const void *k, const void *v, int64_t kv_token_s
  *   out           device [num_seqs, num_q_heads, head_dim] of out_dtype, 16-byte aligned
  *                 (PKV_F32, or the cache's dtype).
  *   workspace     device scratch of >= pkv_attn_decode_workspace_size bytes,
- *                 256-byte aligned; its contents on entry do not matter.
+ *                 256-byte aligned; its contents on entry do not matter.  That
+ *                 size covers the 16-bit, windowed and int8 decode calls alike.
  */
 PKV_API pkv_status pkv_attn_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                                   int32_t num_kv_heads, int32_t head_dim,

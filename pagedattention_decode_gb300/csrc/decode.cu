@@ -148,7 +148,7 @@ __device__ __forceinline__ int range_owner(int64_t x, int64_t total, int64_t cta
 }
 
 template <int D, typename T, bool I8>
-__global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), 1)
+__global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
     decode_splitk_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                          const DecodeParams p) {
     // 2 KB shared tiles per KV head per sub-block: 16 tokens x 64 dims of a
@@ -715,10 +715,13 @@ static pkv_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, 
     if (st != PKV_OK) return st;
     pl->heads_per_cta = pick_heads_per_cta(hkv, head_dim, i8);
     pl->num_hg = hkv / pl->heads_per_cta;
-    // persistent: all CTAs (one per SM over all head groups) resident at once
-    pl->cmax = sms / pl->num_hg > 0 ? sms / pl->num_hg : 1;
+    // persistent: all CTAs resident at once -- one per SM over all head
+    // groups, two per SM for int8 (half-size stages: more consumer warps per
+    // SM to hide the code conversion)
+    const int per_sm = i8 ? 2 : 1;
+    pl->cmax = per_sm * sms / pl->num_hg > 0 ? per_sm * sms / pl->num_hg : 1;
     const int stage_bytes = pl->heads_per_cta * (i8 ? 1 : head_dim / 64) * 2 * kTile;
-    int ns = (200 * 1024) / stage_bytes;
+    int ns = (200 * 1024 / per_sm) / stage_bytes;
     pl->stages = ns > 16 ? 16 : (ns < 2 ? 2 : ns);
     pl->threads = 32 * (1 + pl->heads_per_cta);
     // stages, alignment slack, barriers, and (int8) two scale rows per stage; <= 210 KB (set once per device)
@@ -871,12 +874,27 @@ static pkv_status run_decode_i8(const void *q, int64_t q_stride, const pkv_cache
                                     : launch_decode_t<128, __half, true>(mk, mv, p, pl, stream);
 }
 
+// Workspace of the 16-bit decode plan (the no-allocation entry point sizes its call with this).
 pkv_status decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, int32_t head_dim,
                                  int32_t device, size_t *bytes) {
     DecodePlan pl;
     pkv_status st = make_plan(num_seqs, num_q_heads, hkv, head_dim, device, &pl);
     if (st != PKV_OK) return st;
     *bytes = pl.meta_bytes + pl.ml_bytes + pl.o_bytes;
+    return PKV_OK;
+}
+
+// The larger of the 16-bit and int8 plans: one workspace serves every decode call.
+static pkv_status decode_workspace_size_any(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, int32_t head_dim,
+                                            int32_t device, size_t *bytes) {
+    size_t a = 0;
+    pkv_status st = decode_workspace_size(num_seqs, num_q_heads, hkv, head_dim, device, &a);
+    if (st != PKV_OK) return st;
+    DecodePlan pl;
+    st = make_plan(num_seqs, num_q_heads, hkv, head_dim, device, &pl, true);
+    if (st != PKV_OK) return st;
+    const size_t b = pl.meta_bytes + pl.ml_bytes + pl.o_bytes;
+    *bytes = a > b ? a : b;
     return PKV_OK;
 }
 
@@ -910,7 +928,7 @@ pkv_status pkv_attn_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                           int32_t head_dim, int32_t device, size_t *bytes) {
     PKV_CHECK_ARG(bytes && num_seqs >= 0 && num_kv_heads > 0 && num_q_heads > 0 && head_dim > 0,
                   PKV_ERR_INVALID_ARG, "bad argument");
-    pkv_status st = decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, device, bytes);
+    pkv_status st = decode_workspace_size_any(num_seqs, num_q_heads, num_kv_heads, head_dim, device, bytes);
     return st == PKV_OK ? ok() : st;
 }
 
