@@ -356,9 +356,34 @@ def time_device_graph(step: DecodeStep, steps: int, warmup: int, barrier):
     return start.elapsed_time(end), dec_eager, [], clk.summary()
 
 
-def time_e2e(w: W.Workload, step: DecodeStep, steps: int, warmup: int, barrier, use_graph: bool = True):
-    """Public-API step with host buffers: allocator -> pinned host -> H2D ->
-    write + decode -> D2H of the output, all inside the timed region."""
+def _blob_layout(parts):
+    """Byte offsets of named tensors packed into one buffer (256-byte aligned)."""
+    off, lay = 0, {}
+    for name, (shape, dtype) in parts.items():
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        lay[name] = (off, n, shape, dtype)
+        off += (n + 255) // 256 * 256
+    return lay, off
+
+
+def _views(blob, lay):
+    return {name: blob[o:o + n].view(dt).view(shape) for name, (o, n, shape, dt) in lay.items()}
+
+
+def time_e2e(w: W.Workload, step: DecodeStep, steps: int, warmup: int, barrier, pipelined: bool = True):
+    """Public-API step with host buffers: host allocator -> pinned host -> H2D ->
+    pkv_write_kv + pkv_attn_decode -> D2H of the output -> host read of that
+    output, all inside the timed region, every step.
+
+    A step's inputs (q, new k/v rows, slot mapping, block tables, lengths) are
+    packed into one pinned buffer and cross in one copy; the output comes back
+    in one copy.  ``pipelined`` runs the loop the way a serving engine does:
+    two buffer sets, the host prepares step i+1 while the GPU runs step i, the
+    input copy of step i+1 and the output copy of step i-1 run on their own
+    streams beside step i's kernels (one CUDA graph per set), and the host
+    waits for step i's output after it has issued step i+1.  Otherwise every
+    step runs on one stream and ends with the host reading its output before
+    the next step starts."""
     P = step.P
     dev = step.dev
     B, hq, hkv, d, bs = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
@@ -367,65 +392,97 @@ def time_e2e(w: W.Workload, step: DecodeStep, steps: int, warmup: int, barrier, 
     seqs = [alloc.create_sequence() for _ in range(B)]
     alloc.append_tokens(seqs, [L - 1 for L in w.lengths])  # cached context before the step
     max_blocks = W.blocks_for(max(w.lengths) + steps + warmup + 4, bs)
-    pin = dict(
-        q=step.q_host.pin_memory(), k=step.k_new_host.pin_memory(), v=step.v_new_host.pin_memory(),
-        slots=torch.empty(B, dtype=torch.int64).pin_memory(),
-        pairs=torch.empty(2 * B, dtype=torch.int64).pin_memory(),
-        tables=torch.empty((B, max_blocks), dtype=torch.int32).pin_memory(),
-        lens=torch.empty(B, dtype=torch.int32).pin_memory(),
-        out=torch.empty((B, hq, d), dtype=torch.float32).pin_memory())
-    dq = torch.empty_like(step.q)
-    dk = torch.empty_like(step.k_new)
-    dv = torch.empty_like(step.v_new)
-    dslots = torch.empty(B, dtype=torch.int64, device=dev)
-    dtables = torch.empty((B, max_blocks), dtype=torch.int32, device=dev)
-    dlens = torch.empty(B, dtype=torch.int32, device=dev)
-    dout = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
-    lens_seen = []
+    lay, nbytes = _blob_layout({
+        "q": (tuple(step.q.shape), step.q.dtype), "k": (tuple(step.k_new.shape), step.k_new.dtype),
+        "v": (tuple(step.v_new.shape), step.v_new.dtype), "slots": ((B,), torch.int64),
+        "tables": ((B, max_blocks), torch.int32), "lens": ((B,), torch.int32)})
+    nsets = 2 if pipelined else 1
 
-    def device_part():
-        dq.copy_(pin["q"], non_blocking=True)
-        dk.copy_(pin["k"], non_blocking=True)
-        dv.copy_(pin["v"], non_blocking=True)
-        dslots.copy_(pin["slots"], non_blocking=True)
-        dtables.copy_(pin["tables"], non_blocking=True)
-        dlens.copy_(pin["lens"], non_blocking=True)
-        P.write_kv(dk, dv, dslots, step.k_cache, step.v_cache)
-        P.attn_decode(dq, step.k_cache, step.v_cache, dtables, dlens, w.scale, out=dout, workspace=step.ws)
-        pin["out"].copy_(dout, non_blocking=True)
+    class Set:
+        def __init__(self):
+            self.hin = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+            self.din = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            self.h, self.d = _views(self.hin, lay), _views(self.din, lay)
+            self.h["q"].copy_(step.q_host)
+            self.h["k"].copy_(step.k_new_host)
+            self.h["v"].copy_(step.v_new_host)
+            self.pairs = torch.empty(2 * B, dtype=torch.int64).pin_memory()
+            self.hout = torch.empty((B, hq, d), dtype=torch.float32).pin_memory()
+            self.dout = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
+            self.in_done, self.comp_done, self.out_done = (torch.cuda.Event() for _ in range(3))
+            self.graph = None
 
-    graph = None
-    if use_graph:
-        # capture on scratch copies of the first step's host inputs; the replays
-        # read whatever the allocator wrote into the pinned buffers
-        alloc.append_tokens_into(seqs, pin["slots"], pin["pairs"])
-        alloc.fill_tables(seqs, max_blocks, pin["tables"], pin["lens"])
-        graph = P.StepGraph(device_part)
+        def kernels(self):
+            P.write_kv(self.d["k"], self.d["v"], self.d["slots"], step.k_cache, step.v_cache)
+            P.attn_decode(self.d["q"], step.k_cache, step.v_cache, self.d["tables"], self.d["lens"], w.scale,
+                          out=self.dout, workspace=step.ws)
 
-    def one():
-        npairs = alloc.append_tokens_into(seqs, pin["slots"], pin["pairs"])
+    sets = [Set() for _ in range(nsets)]
+    lens_seen, checksum = [], []
+    compute = torch.cuda.current_stream()
+    copy_in, copy_out = (torch.cuda.Stream() for _ in range(2)) if pipelined else (compute, compute)
+
+    def host_part(s):
+        npairs = alloc.append_tokens_into(seqs, s.h["slots"], s.pairs)
         assert npairs == 0
-        alloc.fill_tables(seqs, max_blocks, pin["tables"], pin["lens"])
-        lens_seen.append(int(pin["lens"].sum()))
-        if graph is not None:
-            graph.replay()
-        else:
-            device_part()
-        torch.cuda.current_stream().synchronize()  # the host reads the step's result
+        alloc.fill_tables(seqs, max_blocks, s.h["tables"], s.h["lens"])
+        lens_seen.append(int(s.h["lens"].sum()))
 
-    for _ in range(warmup):
-        one()
+    for s in sets:  # captured on the first step's inputs; replays read the set's device buffers
+        host_part(s)
+        s.din.copy_(s.hin)
+        s.graph = P.StepGraph(s.kernels)
+    for s in sets:
+        for e in (s.in_done, s.comp_done, s.out_done):
+            e.record(compute)
+    torch.cuda.synchronize()
+
+    def launch(i):
+        s = sets[i % nsets]
+        s.in_done.synchronize()  # the pinned inputs of this set's previous step have been copied
+        host_part(s)
+        copy_in.wait_event(s.comp_done)  # the set's device inputs are no longer read
+        with torch.cuda.stream(copy_in):
+            s.din.copy_(s.hin, non_blocking=True)
+        s.in_done.record(copy_in)
+        compute.wait_event(s.in_done)
+        compute.wait_event(s.out_done)  # the set's previous output has left the device
+        s.graph.replay()
+        s.comp_done.record(compute)
+        copy_out.wait_event(s.comp_done)
+        with torch.cuda.stream(copy_out):
+            s.hout.copy_(s.dout, non_blocking=True)
+        s.out_done.record(copy_out)
+
+    def read(i):
+        s = sets[i % nsets]
+        s.out_done.synchronize()  # the host reads the step's result
+        checksum.append(float(s.hout[0, 0, 0]))
+
+    def run(n):
+        if pipelined:
+            launch(0)
+            for i in range(1, n):
+                launch(i)
+                read(i - 1)
+            read(n - 1)
+        else:
+            for i in range(n):
+                launch(i)
+                read(i)
+
+    run(warmup)
     lens_seen.clear()
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
+    run(steps)
     torch.cuda.synchronize()
     t1 = time.perf_counter()
     barrier()
-    h2d = sum(pin[k].numel() * pin[k].element_size() for k in ("q", "k", "v", "slots", "tables", "lens"))
-    d2h = pin["out"].numel() * pin["out"].element_size()
+    assert len(lens_seen) == steps and all(np.isfinite(checksum))
+    h2d = sum(n for (_, n, _, _) in lay.values())
+    d2h = sets[0].hout.numel() * sets[0].hout.element_size()
     kv_total = sum(lens_seen) * kv_bytes_per_token(hkv, d, 2)
     other = B * hq * d * (2 + 4) + write_bytes(B, hkv, d, 2)
     bytes_total = kv_total + steps * other
@@ -770,13 +827,16 @@ def main():
         "gpu_launches": args.steps * 3 * w.layers,
     }
     if not args.no_e2e and w.layers == 1 and args.workload != "gqa_int8":
-        e2e_ms, e2e_bytes, h2d, d2h = time_e2e(w, step, max(1, min(args.steps, 200)), 3, barrier)
         n_e2e = max(1, min(args.steps, 200))
+        ser_ms, _, _, _ = time_e2e(w, step, n_e2e, 3, barrier, pipelined=False)
+        e2e_ms, e2e_bytes, h2d, d2h = time_e2e(w, step, n_e2e, 3, barrier)
         line["e2e"] = {"value": world * e2e_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / n_e2e, "steps": n_e2e,
                        "tokens_per_s": world * w.batch * n_e2e / (e2e_ms * 1e-3),
-                       "path": "host allocator -> [CUDA graph: pinned H2D -> pkv_write_kv -> pkv_attn_decode "
-                               "-> D2H] -> host sync"}
+                       "path": "host allocator -> one pinned H2D of the packed inputs -> [CUDA graph: "
+                               "pkv_write_kv -> pkv_attn_decode] -> one D2H of the output -> host read; two buffer "
+                               "sets: host work and both copies of neighbouring steps overlap step i's kernels",
+                       "serial_ms_per_step": ser_ms / n_e2e}
     if rank == 0 and not args.no_cpu_baseline:
         rate, n, dt, cores = oracle_sample_rate(w, 5.0)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
