@@ -75,13 +75,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-pkv_status encode_pool_map(CUtensorMap *map, void *base, const pkv_cache *c) {
+pkv_status encode_pool_map(CUtensorMap *map, void *base, const pkv_cache *c, int rows) {
     auto fn = encode_fn();
     PKV_CHECK_ARG(fn, PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    PKV_CHECK_ARG(rows == 16 || rows == 32 || rows == 64 || rows == 128, PKV_ERR_INVALID_ARG, "pool box of %d rows", rows);
     const int tiles = c->num_kv_heads * c->head_dim / 64;
     cuuint64_t dims[3] = {64, (cuuint64_t)tiles, (cuuint64_t)c->num_blocks * c->block_size};
     cuuint64_t strides[2] = {128, (cuuint64_t)c->num_kv_heads * c->head_dim * 2};
-    cuuint32_t box[3] = {64, 1, 16};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                     3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -35,8 +35,9 @@ pkv_status set_smem_once(const void *kernel, int bytes, std::atomic<uint64_t> *d
 
 // 3-D tensor map over a pool seen as [rows = num_blocks * block_size]
 // x [num_kv_heads * head_dim / 64 tiles of 64 elements] x [64 elements], box
-// = 16 rows x 1 tile x 64 elements, 128-byte swizzle (a 2 KB shared tile).
-pkv_status encode_pool_map(CUtensorMap *map, void *base, const pkv_cache *c);
+// = `rows` (16, 32, 64 or 128) rows x 1 tile x 64 elements, 128-byte swizzle
+// (a 2 to 16 KB shared tile).
+pkv_status encode_pool_map(CUtensorMap *map, void *base, const pkv_cache *c, int rows = 16);
 
 // The same for an int8 pool with head_dim 128: box = 16 rows x 1 head x 128
 // codes (one 2 KB shared tile per KV head per 16 tokens).

@@ -7,26 +7,32 @@
 // kv_len keys sees keys t <= kv_len - q_len + i.  For a chunk the work is a
 // dense contraction, so it runs here as a FlashAttention-style loop on UMMA:
 //
-//  * CTA = 128 M rows: the G query heads of one KV head x 128/G query
-//    positions (row r -> head r / (128/G), position q0 + r % (128/G)), so every
-//    K/V tile staged in shared memory serves all G heads.
-//  * Warp 0 streams Q once and then 64-token K and V tiles of the KV head
-//    (TMA, 16 tokens x 64 dims x 128-byte swizzle per box, through the block
-//    table) into a 2-stage ring.
-//  * Warp 1, one thread, issues the MMAs: S = Q K^T (M 128, N 64, K 16 steps,
-//    both operands K-major from shared memory) into one of two TMEM score
-//    buffers, and O += P V (A = P read from TMEM, B = V as an MN-major shared
-//    operand, N = head_dim) into a TMEM accumulator.  Completion is signalled
-//    with tcgen05.commit on mbarriers.
-//  * Warps 2-5 (one TMEM lane = one M row per thread) read scores from TMEM,
-//    apply the causal limit, keep the running max and sum in registers, and
-//    write P back over the scores as a 16-bit hi + lo pair (two MMAs keep
-//    ~16 significant bits of P).  The running max is only moved when it grows
-//    by more than 2^8; then those rows of O are rescaled in TMEM after the
-//    previous P V has completed.  The final O row is divided by the sum and
-//    stored.
-// Two CTAs share an SM (256 TMEM columns and ~97 KB of shared memory each),
-// so one CTA's softmax overlaps the other's MMAs.
+//  * A q tile = 128 M rows: the G query heads of one KV head x 128/G query
+//    positions (row r -> head r / (128/G), position q0 + r % (128/G)).  A CTA
+//    holds two consecutive tiles, so every K/V tile staged in shared memory
+//    serves 256 rows.
+//  * Warp 0 streams Q of both tiles once, then 128-token K and V tiles of the
+//    KV head (TMA through the block table, 128-byte swizzle, boxes of the
+//    largest of 128, 64, 32 or 16 rows that divides block_size: L2 -> shared
+//    throughput grows with the box) into separate K and V rings, so a K tile
+//    is released as soon as the scores that read it are done.
+//  * Warp 1, one thread, issues the MMAs: S = Q K^T (M 128, N 128, K 16
+//    steps, both operands K-major from shared memory) into the tile's TMEM
+//    score columns, and O += P V (A = P read from TMEM, B = V as an MN-major
+//    shared operand, N = head_dim) into its TMEM accumulator.  Per step it
+//    issues P V of tile 0, the next scores of tile 0, P V of tile 1, the next
+//    scores of tile 1: while one tile's softmax runs, the tensor pipe works
+//    on the other tile.  Completion is signalled with tcgen05.commit.
+//  * Warps 4-7 (tile 0) and 8-11 (tile 1), one TMEM lane = one M row per
+//    thread, read the 128 scores of their row with a single wait for the
+//    TMEM loads, apply the causal and window limits, keep the
+//    running max and sum in registers, and write P back over the scores as
+//    16-bit values (bf16: a hi + lo pair, ~16 significant bits).  The running
+//    max is only moved when it grows by more than 2^8; then that row of O is
+//    rescaled in TMEM.  The final O row is divided by the sum and stored.
+// One CTA per SM: all 512 TMEM columns (per tile: S/P 128, O head_dim) and
+// ~197 KB of shared memory; setmaxnreg moves registers from the producer /
+// MMA warpgroup (warps 0-3) to the two softmax warpgroups.
 #include <cuda.h>
 
 #include "launch.h"
@@ -36,9 +42,9 @@ namespace pkv {
 
 namespace {
 
-constexpr int kTok = 64;          // keys per score tile
-constexpr int kStages = 2;
-constexpr int kTmemCols = 256;    // S0 [0,64) S1 [64,128) O [128, 128 + D)
+constexpr int kTok = 128;         // keys per step: the N of the score MMA
+constexpr int kTiles = 2;         // q tiles of 128 M rows per CTA; every K/V stage serves both
+constexpr int kTmemCols = 512;    // 256 columns per tile: scores / P at +0 (128), O at +128 (D)
 constexpr float kRescaleLog2 = 8.f;
 
 template <typename T>
@@ -51,6 +57,8 @@ struct IsBf16<__nv_bfloat16> {
 };
 
 struct TcParams {
+    const void *q;
+    int64_t q_stride;  // elements between query rows
     const int32_t *tables;
     int32_t max_blocks;
     const int32_t *seq_lens;
@@ -60,8 +68,9 @@ struct TcParams {
     void *out;
     int32_t out_f32;
     int32_t *err;
-    int32_t q_tiles;
+    int32_t q_tiles;  // pairs of q tiles per sequence (kTiles * 128 / group positions each)
     int32_t window;   // > 0: each row attends only its most recent `window` keys
+    int32_t box_rows; // rows per K/V TMA box: 128, 64, 32 or 16, a divisor of block_size
 };
 
 // UMMA shared-memory descriptor, 128-byte swizzle (sm_100 family layout:
@@ -123,69 +132,117 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 }  // namespace
 
+template <int D>
+__host__ __device__ constexpr int prefill_stages() {  // stages of the K ring and of the V ring
+    return D == 64 ? 4 : 2;
+}
+
+// Registers per thread after the warpgroups re-balance them: the producer /
+// MMA warpgroup gives registers back, the two softmax warpgroups (a whole
+// row of 128 fp32 scores each per thread) take them.  Their sum must fit the
+// launch's registers (kThreads x the kernel's count): checked on the host.
+constexpr int kThreads = 384;
+constexpr int kRegsLow = 72;
+constexpr int kRegsHigh = 216;
+constexpr int kRegsAtLaunchMin = (128 * kRegsLow + 256 * kRegsHigh + kThreads - 1) / kThreads;
+
 template <int D, typename T>
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const TcParams p) {
     constexpr int HALVES = D / 64;
+    constexpr int S = prefill_stages<D>();
     constexpr int QHALF = 128 * 128;            // bytes of 128 rows x 64 dims
-    constexpr int KVHALF = kTok * 128;           // bytes of 64 tokens x 64 dims
-    constexpr int STAGE = 2 * HALVES * KVHALF;   // K then V
+    constexpr int QTILE = HALVES * QHALF;
+    constexpr int KVHALF = kTok * 128;           // bytes of 128 tokens x 64 dims
+    constexpr int KVSTAGE = HALVES * KVHALF;     // one K (or V) tile
     constexpr bool BF = IsBf16<T>::value;
+    // P enters P V as a 16-bit operand.  fp16 keeps 11 significant bits of each
+    // p in [0, 2^8] (relative error <= 2^-12, far inside the 2e-3 gate); bf16
+    // keeps only 8, so there P is split into hi + lo halves and P V takes two
+    // MMAs per K step.  P of keys 32c .. 32c + 31 lies in TMEM columns
+    // 16c .. 16c + 15 (fp16), or hi in 32c .. 32c + 15 and lo in 32c + 16 ..
+    // 32c + 31 (bf16): columns whose scores have already been read.
+    constexpr bool LO = BF;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bars[2 + 2 * kStages + 6];
+    __shared__ uint64_t bars[1 + 4 * S + 3 * kTiles + 1];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sq = base;
-    uint8_t *skv = base + HALVES * QHALF;
+    uint8_t *sk = base + kTiles * QTILE;
+    uint8_t *sv = sk + S * KVSTAGE;
     uint64_t *q_full = &bars[0];
-    uint64_t *kv_full = &bars[1];
-    uint64_t *kv_empty = &bars[1 + kStages];
-    uint64_t *s_full = &bars[1 + 2 * kStages];
-    uint64_t *p_full = s_full + 2;
-    uint64_t *o_done = p_full + 2;
-    uint64_t *fin = o_done + 2;  // abort path: completion of every MMA issued
+    uint64_t *k_full = &bars[1];
+    uint64_t *k_empty = &bars[1 + S];
+    uint64_t *v_full = &bars[1 + 2 * S];
+    uint64_t *v_empty = &bars[1 + 3 * S];
+    uint64_t *tile_bars = &bars[1 + 4 * S];  // per tile: s_full, p_full, o_done
+    uint64_t *fin = &bars[1 + 4 * S + 3 * kTiles];  // abort path: completion of every MMA issued
+    auto s_full = [&](int u) { return tile_bars + u * 3; };
+    auto p_full = [&](int u) { return tile_bars + u * 3 + 1; };
+    auto o_done = [&](int u) { return tile_bars + u * 3 + 2; };
 
     const int s = blockIdx.y;
     const int kvh = blockIdx.z;
-    const int tile = p.q_tiles - 1 - blockIdx.x;  // longest causal tiles first
+    const int pair = p.q_tiles - 1 - blockIdx.x;  // longest causal tiles first
     const int q_begin = p.cu_q[s];
     const int q_len = p.cu_q[s + 1] - q_begin;
     const int kv_len = p.seq_lens[s];
     const int G = p.group;
-    const int R = 128 / G;                        // query positions per CTA
-    const int q0 = tile * R;
-    if (q_len <= 1 || q0 >= q_len) return;
+    const int R = 128 / G;                        // query positions per tile
+    if (q_len <= 1 || pair * kTiles * R >= q_len) return;
     if (q_len > kv_len || (int64_t)kv_len > (int64_t)p.max_blocks * p.block_size) {
         if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0) set_err(p.err, PKV_DEVERR_LENGTH);
         return;
     }
-    const int last_row = min(q_len, q0 + R) - 1;
-    const int kv_hi = p.causal ? kv_len - q_len + last_row + 1 : kv_len;
-    // window: the CTA's first row has the lowest first key of its rows
-    const int lim_first = p.causal ? kv_len - q_len + q0 : kv_len - 1;
+    // tile u holds positions q0(u) .. q0(u) + R - 1; the window's first key is
+    // lowest for the first row of tile 0, so both tiles walk from j_first
+    const int q00 = pair * kTiles * R;
+    const int lim_first = p.causal ? kv_len - q_len + q00 : kv_len - 1;
     const int lo_first = (p.window > 0 && lim_first - p.window + 1 > 0) ? lim_first - p.window + 1 : 0;
     const int j_first = lo_first / kTok;
-    const int nt = (kv_hi + kTok - 1) / kTok - j_first;
+    auto tile_steps = [&](int u) -> int {
+        const int q0 = q00 + u * R;
+        if (q0 >= q_len) return 0;
+        const int last_row = min(q_len, q0 + R) - 1;
+        const int kv_hi = p.causal ? kv_len - q_len + last_row + 1 : kv_len;
+        return (kv_hi + kTok - 1) / kTok - j_first;
+    };
+    const int nt0 = tile_steps(0), nt1 = tile_steps(1);
+    const int nt = max(nt0, nt1);
+    auto steps_of = [&](int u) { return u ? nt1 : nt0; };
+    // V rows past kv_len (only in the last step) are cleared by the first tile
+    // whose P V reads that step
+    const int zt = nt0 == nt ? 0 : 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         s_abort = 0;
         mbar_init(q_full, 1);
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&kv_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 128);
-            mbar_init(&o_done[i], 1);
+        for (int u = 0; u < kTiles; ++u) {
+            mbar_init(s_full(u), 1);
+            mbar_init(p_full(u), 128);
+            mbar_init(o_done(u), 1);
         }
         mbar_init(fin, 1);
         fence_barrier_init();
@@ -199,166 +256,205 @@ __global__ void __launch_bounds__(192, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0) {
-        // ===== producer: Q once, then K/V tiles =====
+        // ===== producer: Q of both tiles once, then K and V tiles =====
         const uint64_t pol_q = policy_evict_first();
         const uint64_t pol_kv = policy_evict_last();  // re-read by the other q tiles of the chunk
+        const int ntiles = nt1 > 0 ? 2 : 1;
         if (lane == 0) {
             prefetch_tensormap(&tmq);
             prefetch_tensormap(&tmk);
             prefetch_tensormap(&tmv);
-            mbar_arrive_expect_tx(q_full, (uint32_t)(G * HALVES * R * 128));
+            mbar_arrive_expect_tx(q_full, (uint32_t)(ntiles * G * HALVES * R * 128));
         }
         __syncwarp();
-        for (int t = lane; t < G * HALVES; t += 32) {
-            const int g = t / HALVES, half = t % HALVES;
-            tma_load_3d(sq + half * QHALF + g * R * 128, &tmq, q_full, 0, (kvh * G + g) * HALVES + half, q_begin + q0,
-                        pol_q);
+        for (int t = lane; t < ntiles * G * HALVES; t += 32) {
+            const int u = t / (G * HALVES), g = (t / HALVES) % G, half = t % HALVES;
+            tma_load_3d(sq + u * QTILE + half * QHALF + g * R * 128, &tmq, q_full, 0, (kvh * G + g) * HALVES + half,
+                        q_begin + q00 + u * R, pol_q);
         }
         const int32_t *trow = p.tables + (int64_t)s * p.max_blocks;
-        int issued = 0;
+        const int box = p.box_rows;
+        // a tile has at most (128 / 16) * HALVES <= 16 boxes: lane t issues box t
+        // of K and of V (sub-block t / HALVES, half t % HALVES).  Its block-table
+        // entry is read one step ahead, off the issue path.
+        auto boxes_of = [&](int j) {
+            const int nvalid = min(kTok, kv_len - (j_first + j) * kTok);
+            return ((nvalid + box - 1) / box) * HALVES;
+        };
+        auto lookup = [&](int j) -> int {
+            if (j >= nt || lane >= boxes_of(j)) return 0;
+            const int tok = (j_first + j) * kTok + (lane / HALVES) * box;
+            return trow[tok / p.block_size];
+        };
+        int phys_next = lookup(0);
+        int issued_k = 0, issued_v = 0;
         for (int j = 0; j < nt; ++j) {
-            const int stage = j % kStages;
-            int okw = 1;
-            if (lane == 0) okw = mbar_wait(&kv_empty[stage], ((j / kStages) & 1) ^ 1, &s_abort);
-            okw = __shfl_sync(0xffffffffu, okw, 0);
-            if (!okw) {
-                if (lane == 0) {
-                    s_abort = 1;
-                    set_err(p.err, PKV_DEVERR_TIMEOUT);
-                }
-                break;
-            }
+            const int stage = j % S;
+            int phys = phys_next;
+            phys_next = lookup(j + 1);
+            const int nbox = boxes_of(j);
             const int t0 = (j_first + j) * kTok;
-            const int nvalid = min(kTok, kv_len - t0);
-            const int nsub = (nvalid + 15) / 16;
-            if (lane == 0) mbar_arrive_expect_tx(&kv_full[stage], (uint32_t)(nsub * 2 * HALVES * 2048));
-            __syncwarp();
-            for (int t = lane; t < nsub * 2 * HALVES; t += 32) {
-                const int sub = t / (2 * HALVES), r = t % (2 * HALVES);
-                const int which = r / HALVES, half = r % HALVES;
-                const int tok = t0 + sub * 16;
+            int row = 0;
+            if (lane < nbox) {
+                const int tok = t0 + (lane / HALVES) * box;  // box | block_size: a box never leaves its block
                 const int lb = tok / p.block_size;
-                int phys = trow[lb];
                 if (phys < 0 || phys >= p.num_blocks) {
                     set_err(p.err, PKV_DEVERR_BLOCK);
                     phys = 0;
                 }
-                const int row = phys * p.block_size + (tok - lb * p.block_size);
-                uint8_t *dst = skv + stage * STAGE + which * (HALVES * KVHALF) + half * KVHALF + sub * 2048;
-                tma_load_3d(dst, which ? &tmv : &tmk, &kv_full[stage], 0, kvh * HALVES + half, row, pol_kv);
+                row = phys * p.block_size + (tok - lb * p.block_size);
             }
-            issued = j + 1;
+            const uint32_t dst_off = (uint32_t)(stage * KVSTAGE + (lane % HALVES) * KVHALF + (lane / HALVES) * box * 128);
+            int okw = 1;
+            if (lane == 0) okw = mbar_wait(&k_empty[stage], ((j / S) & 1) ^ 1, &s_abort);
+            if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+            if (lane == 0) mbar_arrive_expect_tx(&k_full[stage], (uint32_t)(nbox * box * 128));
+            __syncwarp();
+            if (lane < nbox) tma_load_3d(sk + dst_off, &tmk, &k_full[stage], 0, kvh * HALVES + lane % HALVES, row, pol_kv);
+            issued_k = j + 1;
+            if (lane == 0) okw = mbar_wait(&v_empty[stage], ((j / S) & 1) ^ 1, &s_abort);
+            if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+            if (lane == 0) mbar_arrive_expect_tx(&v_full[stage], (uint32_t)(nbox * box * 128));
+            __syncwarp();
+            if (lane < nbox) tma_load_3d(sv + dst_off, &tmv, &v_full[stage], 0, kvh * HALVES + lane % HALVES, row, pol_kv);
+            issued_v = j + 1;
         }
-        if (s_abort && lane == 0) {
-            // the loads this warp issued must land before the CTA exits
+        if (issued_v < nt && lane == 0) {
+            // gave up: the loads this warp issued must land before the CTA exits
+            s_abort = 1;
+            set_err(p.err, PKV_DEVERR_TIMEOUT);
             volatile int never = 0;
             mbar_wait(q_full, 0, &never);
-            for (int k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
-                mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, &never);
+            for (int k = issued_k > S ? issued_k - S : 0; k < issued_k; ++k)
+                mbar_wait(&k_full[k % S], (k / S) & 1, &never);
+            for (int k = issued_v > S ? issued_v - S : 0; k < issued_v; ++k)
+                mbar_wait(&v_full[k % S], (k / S) & 1, &never);
         }
     } else if (warp == 1) {
         // ===== MMA issuer =====
         if (lane == 0) {
             const uint32_t idS = idesc_f16(BF ? 1 : 0, 0, 128, kTok);
             const uint32_t idPV = idesc_f16(BF ? 1 : 0, 1, 128, D);
-            const uint32_t sq_a = smem_u32(sq), skv_a = smem_u32(skv);
-            bool ok = mbar_wait(q_full, 0, &s_abort);
-            auto issue_pv = [&](int i) -> bool {
-                const int b = i & 1, stage = i % kStages;
-                if (!mbar_wait(&p_full[b], (i >> 1) & 1, &s_abort)) return false;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kTok / 16; ++kk) {
-                    const uint64_t vd = sw128_desc(skv_a + stage * STAGE + HALVES * KVHALF + kk * 2048, KVHALF, 1024);
-                    umma_ts(tmem + 128, tmem + b * 64 + kk * 8, vd, idPV, (i > 0 || kk > 0) ? 1u : 0u);
-                    umma_ts(tmem + 128, tmem + b * 64 + 32 + kk * 8, vd, idPV, 1u);
-                }
-                umma_commit(&o_done[b]);
-                umma_commit(&kv_empty[stage]);
-                return true;
-            };
-            for (int j = 0; j < nt && ok; ++j) {
-                const int stage = j % kStages, b = j & 1;
-                ok = mbar_wait(&kv_full[stage], (j / kStages) & 1, &s_abort);
-                if (ok && j >= 2) ok = mbar_wait(&o_done[b], ((j - 2) >> 1) & 1, &s_abort);
-                if (!ok) break;
-                tc_fence_after();
+            const uint32_t sq_a = smem_u32(sq), sk_a = smem_u32(sk), sv_a = smem_u32(sv);
+            auto issue_s = [&](int u, int j) {
+                const uint32_t kst = sk_a + (j % S) * KVSTAGE;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const int half = kk >> 2, koff = (kk & 3) * 32;
-                    const uint64_t ad = sw128_desc(sq_a + half * QHALF + koff, 16, 1024);
-                    const uint64_t bd = sw128_desc(skv_a + stage * STAGE + half * KVHALF + koff, 16, 1024);
-                    umma_ss(tmem + b * 64, ad, bd, idS, kk > 0 ? 1u : 0u);
+                    const uint64_t ad = sw128_desc(sq_a + u * QTILE + half * QHALF + koff, 16, 1024);
+                    const uint64_t bd = sw128_desc(kst + half * KVHALF + koff, 16, 1024);
+                    umma_ss(tmem + u * 256, ad, bd, idS, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(&s_full[b]);
-                if (j >= 1) ok = issue_pv(j - 1);
+                umma_commit(s_full(u));
+            };
+            auto issue_pv = [&](int u, int j) {
+                const uint32_t vst = sv_a + (j % S) * KVSTAGE;
+                const uint32_t ts = tmem + u * 256, to = tmem + u * 256 + 128;
+#pragma unroll
+                for (int kk = 0; kk < kTok / 16; ++kk) {
+                    const uint64_t vd = sw128_desc(vst + kk * 2048, KVHALF, 1024);
+                    const uint32_t col = LO ? (kk >> 1) * 32 + (kk & 1) * 8 : kk * 8;
+                    umma_ts(to, ts + col, vd, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    if (LO) umma_ts(to, ts + col + 16, vd, idPV, 1u);
+                }
+                umma_commit(o_done(u));
+            };
+            bool ok = mbar_wait(q_full, 0, &s_abort) && mbar_wait(&k_full[0], 0, &s_abort);
+            if (ok) {
+                tc_fence_after();
+                for (int u = 0; u < kTiles; ++u)
+                    if (steps_of(u) > 0) issue_s(u, 0);
+                umma_commit(&k_empty[0]);
             }
-            if (ok) ok = issue_pv(nt - 1);
+            for (int j = 0; j < nt && ok; ++j) {
+                const uint32_t ph = j & 1;
+                const int j1 = j + 1;
+                bool v_ready = false, k_ready = false;
+                for (int u = 0; u < kTiles && ok; ++u) {
+                    if (j >= steps_of(u)) continue;
+                    ok = mbar_wait(p_full(u), ph, &s_abort);
+                    // the last step's V rows past kv_len are cleared by tile zt
+                    if (ok && u != zt && (j_first + j + 1) * kTok > kv_len) ok = mbar_wait(p_full(zt), ph, &s_abort);
+                    if (ok && !v_ready) ok = v_ready = mbar_wait(&v_full[j % S], (j / S) & 1, &s_abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(u, j);
+                    if (j1 < steps_of(u)) {
+                        if (!k_ready) ok = k_ready = mbar_wait(&k_full[j1 % S], (j1 / S) & 1, &s_abort);
+                        // the scores overwrite P of step j: its P V must have completed
+                        if (ok) ok = mbar_wait(o_done(u), ph, &s_abort);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(u, j1);
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&v_empty[j % S]);
+                if (k_ready) umma_commit(&k_empty[j1 % S]);
+            }
             if (!ok) {
                 s_abort = 1;
                 set_err(p.err, PKV_DEVERR_TIMEOUT);
             }
         }
+    }
     } else {
-        // ===== softmax + epilogue: one M row per thread =====
-        const int qw = warp & 3;
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+        // ===== softmax + epilogue: warps 4-7 tile 0, warps 8-11 tile 1, one M row per thread =====
+        const int u = (warp - 4) >> 2;
+        const int ntu = steps_of(u);
+        const int qw = warp & 3;  // a warp reaches TMEM lanes 32 * (warp % 4) .. + 31
         const int row = qw * 32 + lane;
-        const uint32_t trow_addr = tmem + ((uint32_t)(qw * 32) << 16);
+        const uint32_t trow_addr = tmem + ((uint32_t)(qw * 32) << 16) + u * 256;
         const int g = row / R;
-        const int qi = q0 + row % R;
+        const int qi = q00 + u * R + row % R;
         const bool valid = qi < q_len;
         const int lim = (p.causal && valid) ? kv_len - q_len + qi : kv_len - 1;
         const int lo = (p.window > 0 && lim - p.window + 1 > 0) ? lim - p.window + 1 : 0;
         const float sl = p.scale_log2;
         float m_used = -INFINITY, lsum = 0.f;
         bool ok = true;
-        for (int j = 0; j < nt; ++j) {
-            const int b = j & 1;
+        for (int j = 0; j < ntu; ++j) {
             // warp-uniform outcome: the tcgen05 ld/st below are warp-collective
-            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], (j >> 1) & 1, &s_abort))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(s_full(u), j & 1, &s_abort))) {
                 ok = false;
                 break;
             }
+            // the scores of step j were issued after P V of step j - 1 completed,
+            // so O is settled here and may be rescaled
             tc_fence_after();
-            uint32_t sr[64];
-            tmem_ld32(trow_addr + b * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(trow_addr + b * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-            tmem_wait_ld();
             const int t0 = (j_first + j) * kTok;
-            // eight independent partial maxima (short dependency chains);
-            // tiles every row of the warp sees in full skip the causal select
-            float pm[8];
+            // every row of the warp sees every key of the tile: no masking
+            const bool whole = __all_sync(0xffffffffu, t0 + kTok - 1 <= lim && t0 >= lo);
+            // the row's 128 scores, read with one wait (each wait exposes the
+            // whole TMEM load latency)
+            uint32_t sr[kTok];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
-            if (__all_sync(0xffffffffu, t0 + kTok - 1 <= lim && t0 >= lo)) {
-#pragma unroll
-                for (int c = 0; c < kTok; ++c) {
-                    const float x = __uint_as_float(sr[c]) * sl;
-                    sr[c] = __float_as_uint(x);
-                    pm[c & 7] = fmaxf(pm[c & 7], x);
-                }
-            } else {
+            for (int c0 = 0; c0 < kTok; c0 += 32)
+                tmem_ld32(trow_addr + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
+            tmem_wait_ld();
+            if (!whole) {
 #pragma unroll
                 for (int c = 0; c < kTok; ++c) {
-                    const float x = (t0 + c <= lim && t0 + c >= lo) ? __uint_as_float(sr[c]) * sl : -INFINITY;
-                    sr[c] = __float_as_uint(x);
-                    pm[c & 7] = fmaxf(pm[c & 7], x);
+                    const int key = t0 + c;
+                    if (!(key <= lim && key >= lo)) sr[c] = __float_as_uint(-INFINITY);
                 }
             }
+            // the row max of the raw scores (the scale is positive)
+            float pm[8];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) pm[v] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kTok; ++c) pm[c & 7] = fmaxf(pm[c & 7], __uint_as_float(sr[c]));
             const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * sl;
             const float m_new = fmaxf(m_used, mx);
             const bool need = m_new > m_used + kRescaleLog2;
             const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
             if (__any_sync(0xffffffffu, need) && j > 0) {
-                // the previous P V must be complete before its rows are rescaled
-                if (!__all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, &s_abort))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t orr[32];
@@ -368,53 +464,64 @@ __global__ void __launch_bounds__(192, 2)
                     for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
                     tmem_st32(trow_addr + 128 + c0, orr);
                 }
-                tmem_wait_st();
             }
             if (need) {
                 lsum *= alpha;
                 m_used = m_new;
             }
-            uint32_t ph[32], pl[32];
+            // p = 2^(s * scale - m), written back as 16-bit values.  With a
+            // window a row can meet whole tiles before its first key: there
+            // m_used is still -inf and those p must be 0, not NaN.
+            const bool none_yet = m_used == -INFINITY;
+            const float neg_m = -m_used;
             float ps[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) ps[u] = 0.f;
-            // with a window a row can meet whole tiles before its first key:
-            // there m_used is still -inf and those p must be 0, not NaN
-            const bool none_yet = m_used == -INFINITY;
+            for (int v = 0; v < 8; ++v) ps[v] = 0.f;
 #pragma unroll
-            for (int c = 0; c < kTok; c += 2) {
-                float p0 = fast_exp2(__uint_as_float(sr[c]) - m_used);
-                float p1 = fast_exp2(__uint_as_float(sr[c + 1]) - m_used);
-                if (none_yet) {
-                    p0 = 0.f;
-                    p1 = 0.f;
+            for (int c0 = 0; c0 < kTok; c0 += 32) {
+                uint32_t ph[16], pl[16];
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    float p0 = fast_exp2(fmaf(__uint_as_float(sr[c0 + c]), sl, neg_m));
+                    float p1 = fast_exp2(fmaf(__uint_as_float(sr[c0 + c + 1]), sl, neg_m));
+                    if (none_yet) {
+                        p0 = 0.f;
+                        p1 = 0.f;
+                    }
+                    ps[(c >> 1) & 7] += p0 + p1;
+                    const uint32_t h = pack2<T>(p0, p1);
+                    ph[c / 2] = h;
+                    if (LO) {
+                        const float2 hf = unpack2<T>(h);
+                        pl[c / 2] = pack2<T>(p0 - hf.x, p1 - hf.y);
+                    }
                 }
-                ps[(c >> 1) & 7] += p0 + p1;
-                const uint32_t h = pack2<T>(p0, p1);
-                const float2 hf = unpack2<T>(h);
-                ph[c / 2] = h;
-                pl[c / 2] = pack2<T>(p0 - hf.x, p1 - hf.y);
+                if (LO) {
+                    tmem_st16(trow_addr + c0, ph);
+                    tmem_st16(trow_addr + c0 + 16, pl);
+                } else {
+                    tmem_st16(trow_addr + c0 / 2, ph);
+                }
             }
             lsum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-            tmem_st32(trow_addr + b * 64, ph);
-            tmem_st32(trow_addr + b * 64 + 32, pl);
-            // V rows past kv_len in this tile hold stale or unrelated data: zero them
-            if (t0 + kTok > kv_len) {
-                const int rr = row & (kTok - 1), half = row / kTok;
-                if (half < HALVES && rr >= kv_len - t0) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(skv + (j % kStages) * STAGE + HALVES * KVHALF +
-                                                           half * KVHALF + rr * 128);
+            // V rows past kv_len in the last tile hold stale or unrelated data: zero them
+            if (u == zt && t0 + kTok > kv_len) {
+                if (row >= kv_len - t0) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+                    for (int half = 0; half < HALVES; ++half) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(sv + (j % S) * KVSTAGE + half * KVHALF + row * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&p_full[b]);
+            mbar_arrive(p_full(u));
         }
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, &s_abort));
-        if (ok) {
+        if (ok && ntu > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done(u), (ntu - 1) & 1, &s_abort));
+        if (ok && ntu > 0) {
             tc_fence_after();
             const float inv = 1.f / lsum;
             const int64_t hq = (int64_t)p.hkv * G;
@@ -443,7 +550,7 @@ __global__ void __launch_bounds__(192, 2)
                     }
                 }
             }
-        } else if (lane == 0) {
+        } else if (ntu > 0 && lane == 0) {
             s_abort = 1;
             set_err(p.err, PKV_DEVERR_TIMEOUT);
         }
@@ -469,14 +576,25 @@ template <int D, typename T>
 static pkv_status launch_prefill_tc_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                                       const TcParams &p, int num_seqs, cudaStream_t stream) {
     constexpr int HALVES = D / 64;
-    // + 1 KB for the 1024-byte alignment of the swizzled tiles, + 4 KB of slack after the last stage
-    const int smem = HALVES * 128 * 128 + kStages * 2 * HALVES * kTok * 128 + 1024 + 4096;
+    // Q of both tiles + the K and V rings, + 1 KB for the 1024-byte alignment
+    // of the swizzled tiles, + 4 KB of slack after the last stage
+    const int smem = kTiles * HALVES * 128 * 128 + 2 * prefill_stages<D>() * HALVES * kTok * 128 + 1024 + 4096;
     auto kern = prefill_tc_kernel<D, T>;
     static std::atomic<uint64_t> smem_set{0};
     pkv_status st = set_smem_once(reinterpret_cast<const void *>(kern), smem, &smem_set);
     if (st != PKV_OK) return st;
     dim3 grid(p.q_tiles, num_seqs, p.hkv);
-    kern<<<grid, 192, smem, stream>>>(mq, mk, mv, p);
+    // the register re-balancing inside the kernel needs at least
+    // kRegsAtLaunchMin registers per thread at launch, or it would wait forever
+    static std::atomic<int> regs{0};
+    if (regs.load() == 0) {
+        cudaFuncAttributes fa{};
+        PKV_CUDA_TRY(cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(kern)));
+        regs.store(fa.numRegs);
+    }
+    PKV_CHECK_ARG(regs.load() >= kRegsAtLaunchMin, PKV_ERR_UNSUPPORTED,
+                  "prefill kernel built with %d registers per thread, needs >= %d", regs.load(), kRegsAtLaunchMin);
+    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, p);
     PKV_CUDA_TRY(cudaGetLastError());
     return PKV_OK;
 }
@@ -504,13 +622,19 @@ pkv_status run_prefill_tc(const void *q, int64_t q_stride, const pkv_cache *cach
     p.err = err_word;
     p.window = window > 0 ? window : 0;
     const int rows = 128 / p.group;
-    p.q_tiles = (max_q_len + rows - 1) / rows;
+    p.q_tiles = (max_q_len + kTiles * rows - 1) / (kTiles * rows);
+    p.box_rows = cache->block_size % 128 == 0  ? 128
+                 : cache->block_size % 64 == 0 ? 64
+                 : cache->block_size % 32 == 0 ? 32
+                                               : 16;
+    p.q = q;
+    p.q_stride = q_stride;
     CUtensorMap mq, mk, mv;
     pkv_status st = encode_q_map(&mq, q, q_stride, total_q, num_q_heads, cache->head_dim, rows, cache->dtype);
     if (st != PKV_OK) return st;
-    st = encode_pool_map(&mk, cache->k, cache);
+    st = encode_pool_map(&mk, cache->k, cache, p.box_rows);
     if (st != PKV_OK) return st;
-    st = encode_pool_map(&mv, cache->v, cache);
+    st = encode_pool_map(&mv, cache->v, cache, p.box_rows);
     if (st != PKV_OK) return st;
     const bool bf = cache->dtype == PKV_BF16;
     if (cache->head_dim == 64)
