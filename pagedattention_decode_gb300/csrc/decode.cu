@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
     float *sscale = reinterpret_cast<float *>(empty + NS);  // int8: [NS][2][hkv] per-stage block scales
     const int hg = blockIdx.y;
     const bool meta_cta = blockIdx.x == 0 && blockIdx.y == 0;
+    pdl_wait();  // the previous kernel on the stream (e.g. the slot write) is complete
 
     // ---- 1. total sub-blocks, this CTA's range ------------------------------
     int64_t total = 0;
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
             set_err(p.err, PKV_DEVERR_TIMEOUT);
         }
         // every load of this CTA is issued: the merge kernel may be scheduled
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        pdl_trigger();
         // drain: the last load issued into each stage must land before the CTA exits
         if (lane == 0) {
             const int first = it > NS ? it - NS : 0;
@@ -577,7 +578,8 @@ constexpr int kMergeThreads = 512;
 template <int D, typename T, int kMergeHeads>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
     extern __shared__ float4 s_merge[];  // [groups][kMergeHeads * D / 4] partial sums, then [parts][heads] weights
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
+    pdl_trigger();
     const int s = blockIdx.x;
     if (p.cu_q && p.cu_q[s + 1] - p.cu_q[s] != 1) return;
     const int64_t qrow = p.cu_q ? (int64_t)p.cu_q[s] : (int64_t)s;
@@ -742,9 +744,8 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     static std::atomic<uint64_t> smem_set{0};
     pkv_status st = set_smem_once(reinterpret_cast<const void *>(kern), 210 * 1024, &smem_set);
     if (st != PKV_OK) return st;
-    dim3 grid(pl.cmax, pl.num_hg);
-    kern<<<grid, pl.threads, pl.smem_bytes, stream>>>(mk, mv, p);
-    PKV_CUDA_TRY(cudaGetLastError());
+    st = launch_pdl(kern, dim3(pl.cmax, pl.num_hg), dim3(pl.threads), (size_t)pl.smem_bytes, stream, mk, mv, p);
+    if (st != PKV_OK) return st;
     // the merge reads only what the decode kernel wrote: launch it as a
     // programmatic dependent so it is scheduled while the decode kernel drains
     // few sequences: 4 query heads per merge CTA (more CTAs share a long

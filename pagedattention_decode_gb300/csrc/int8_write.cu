@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(256) write_kv_int8_kernel(const T *__restrict_
                                                             int32_t D, int32_t *err) {
     __shared__ int32_t src[256];  // offset -> token of its last writer in this run, or -1
     __shared__ int32_t s_min, s_max;
+    pdl_wait();
+    pdl_trigger();
     const int64_t t = blockIdx.x;
     const int64_t nslots = (int64_t)num_blocks * bs;
     const int64_t slot = slots[t];
@@ -180,18 +182,17 @@ pkv_status pkv_write_kv_int8(const void *k, const void *v, int64_t kv_token_stri
     PKV_CHECK_ARG(cache->head_dim % 4 == 0 && aligned16(k) && aligned16(v) && kv_token_stride % 4 == 0,
                   PKV_ERR_INVALID_ARG, "k/v rows must be 16-byte aligned, head_dim a multiple of 4");
     const dim3 grid((unsigned)num_tokens, (unsigned)((2 * cache->num_kv_heads + 7) / 8));
-    if (cache->dtype == PKV_BF16)
-        write_kv_int8_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
-            static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v), kv_token_stride,
-            slot_mapping, num_tokens, cache->k, cache->v, cache->k_scale, cache->v_scale, cache->num_blocks,
-            cache->block_size, cache->num_kv_heads, cache->head_dim, err_word);
-    else
-        write_kv_int8_kernel<__half><<<grid, 256, 0, stream>>>(
-            static_cast<const __half *>(k), static_cast<const __half *>(v), kv_token_stride, slot_mapping, num_tokens,
-            cache->k, cache->v, cache->k_scale, cache->v_scale, cache->num_blocks, cache->block_size,
-            cache->num_kv_heads, cache->head_dim, err_word);
-    PKV_CUDA_TRY(cudaGetLastError());
-    return ok();
+    st =
+        cache->dtype == PKV_BF16
+            ? launch_pdl(write_kv_int8_kernel<__nv_bfloat16>, grid, dim3(256), 0, stream,
+                         static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v), kv_token_stride,
+                         slot_mapping, num_tokens, cache->k, cache->v, cache->k_scale, cache->v_scale,
+                         cache->num_blocks, cache->block_size, cache->num_kv_heads, cache->head_dim, err_word)
+            : launch_pdl(write_kv_int8_kernel<__half>, grid, dim3(256), 0, stream, static_cast<const __half *>(k),
+                         static_cast<const __half *>(v), kv_token_stride, slot_mapping, num_tokens, cache->k,
+                         cache->v, cache->k_scale, cache->v_scale, cache->num_blocks, cache->block_size,
+                         cache->num_kv_heads, cache->head_dim, err_word);
+    return st == PKV_OK ? ok() : st;
 }
 
 }  // extern "C"

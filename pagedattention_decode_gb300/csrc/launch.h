@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <utility>
 
 #include "internal.h"
 
@@ -21,6 +22,28 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
         if (e_ != cudaSuccess)                                                          \
             return pkv::fail(PKV_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_));     \
     } while (0)
+
+// Launches `kernel` as a programmatic dependent of the work before it on the
+// stream: its CTAs may be scheduled while the previous kernel finishes.  Every
+// kernel of this library begins with griddepcontrol.wait (pdl_wait) before it
+// touches global memory, which waits for the whole previous grid and its
+// memory operations, so this is safe after any kernel, ours or the caller's.
+template <typename... KArgs, typename... Args>
+pkv_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                      Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    PKV_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...));
+    return PKV_OK;
+}
 
 // Checks a pool descriptor: pointers, geometry, type.
 pkv_status check_cache(const pkv_cache *c, const char *what);

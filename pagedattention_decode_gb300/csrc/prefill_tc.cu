@@ -196,6 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto p_full = [&](int u) { return tile_bars + u * 3 + 1; };
     auto o_done = [&](int u) { return tile_bars + u * 3 + 2; };
 
+    pdl_wait();  // the previous kernel on the stream (e.g. the slot write) is complete
+    pdl_trigger();
     const int s = blockIdx.y;
     const int kvh = blockIdx.z;
     const int pair = p.q_tiles - 1 - blockIdx.x;  // longest causal tiles first
@@ -594,9 +596,7 @@ static pkv_status launch_prefill_tc_t(const CUtensorMap &mq, const CUtensorMap &
     }
     PKV_CHECK_ARG(regs.load() >= kRegsAtLaunchMin, PKV_ERR_UNSUPPORTED,
                   "prefill kernel built with %d registers per thread, needs >= %d", regs.load(), kRegsAtLaunchMin);
-    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, p);
-    PKV_CUDA_TRY(cudaGetLastError());
-    return PKV_OK;
+    return launch_pdl(kern, grid, dim3(kThreads), (size_t)smem, stream, mq, mk, mv, p);
 }
 
 // Prefill chunks of a varlen call on tcgen05 (rows of q_len == 1 are left to the decode kernel).

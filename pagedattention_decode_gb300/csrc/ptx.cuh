@@ -16,6 +16,12 @@ namespace pkv {
 // Roughly 2 s at GB300 clocks: far above any legitimate wait in these kernels.
 constexpr long long kWaitLimitCycles = 4000000000LL;
 
+// Programmatic dependent launch: wait for the previous grid on the stream
+// (complete, memory visible) before touching global memory; let the next
+// grid be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -16,6 +16,8 @@ namespace pkv {
 __global__ void write_kv_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v, int64_t src_stride16,
                                 const int64_t *__restrict__ slots, int32_t num_tokens, uint4 *__restrict__ kc,
                                 uint4 *__restrict__ vc, int64_t num_slots, int32_t row16, int32_t *err) {
+    pdl_wait();
+    pdl_trigger();
     const int warps = blockDim.x >> 5;
     const int64_t t = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -47,6 +49,8 @@ struct LayerPtrs {
 // grid: x = chunk of the block (16 KB each), y = pair, z = layer
 __global__ void copy_blocks_kernel(LayerPtrs layers, const int64_t *__restrict__ pairs, int32_t num_blocks,
                                    int64_t block16, int32_t chunk16, int32_t *err) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t src = pairs[2 * (int64_t)blockIdx.y];
     const int64_t dst = pairs[2 * (int64_t)blockIdx.y + 1];
     if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
@@ -87,12 +91,12 @@ pkv_status pkv_write_kv(const void *k, const void *v, int64_t kv_token_stride, c
                   "k/v rows must start on 16-byte boundaries");
     const int warps = 8;
     dim3 grid((unsigned)((num_tokens + warps - 1) / warps));
-    write_kv_kernel<<<grid, warps * 32, 0, stream>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), kv_token_stride * 2 / 16, slot_mapping,
-        num_tokens, static_cast<uint4 *>(cache->k), static_cast<uint4 *>(cache->v),
-        (int64_t)cache->num_blocks * cache->block_size, (int32_t)(row * 2 / 16), err_word);
-    PKV_CUDA_TRY(cudaGetLastError());
-    return ok();
+    st = launch_pdl(
+        write_kv_kernel, grid, dim3(warps * 32), 0, stream, static_cast<const uint4 *>(k),
+        static_cast<const uint4 *>(v), (int64_t)(kv_token_stride * 2 / 16), slot_mapping, num_tokens,
+        static_cast<uint4 *>(cache->k), static_cast<uint4 *>(cache->v), (int64_t)cache->num_blocks * cache->block_size,
+        (int32_t)(row * 2 / 16), err_word);
+    return st == PKV_OK ? ok() : st;
 }
 
 pkv_status pkv_copy_blocks(const pkv_cache *caches, int32_t num_layers, const int64_t *src_dst_pairs,
@@ -120,9 +124,9 @@ pkv_status pkv_copy_blocks(const pkv_cache *caches, int32_t num_layers, const in
             lp.v[i] = static_cast<uint4 *>(caches[l0 + i].v);
         }
         dim3 grid(chunks, (unsigned)num_pairs, (unsigned)n);
-        copy_blocks_kernel<<<grid, 256, 0, stream>>>(lp, src_dst_pairs, caches[0].num_blocks, block16, chunk16,
-                                                     err_word);
-        PKV_CUDA_TRY(cudaGetLastError());
+        const pkv_status st = launch_pdl(copy_blocks_kernel, grid, dim3(256), 0, stream, lp, src_dst_pairs,
+                                         caches[0].num_blocks, block16, chunk16, err_word);
+        if (st != PKV_OK) return st;
     }
     return ok();
 }

@@ -80,3 +80,19 @@ def test_sliding_window_varlen(window, causal):
     want = oracle.paged_attention(case.q, case.k_cache, case.v_cache, case.dtype, case.tables.numpy(),
                                   case.lens.numpy(), case.scale, cu_q=case.cu_q.numpy(), causal=causal, window=window)
     assert_close(out, want, what=f"varlen window {window} causal {causal}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("q_sigma", [2.0, 4.0])
+def test_peaked_attention_prefill(dtype, q_sigma):
+    """Large query magnitudes concentrate each row's softmax on a few keys, where
+    the rounding of P to a 16-bit operand of the P V MMA weighs most: the 2e-3
+    gate must still hold (fp16 P keeps 11 significant bits, bf16 a hi + lo pair)."""
+    import dataclasses
+    q_lens = [300, 1, 129]
+    kv_lens = [300 + 700, 900, 129]
+    case = varlen_case(90 + int(q_sigma), q_lens, kv_lens, 32, 8, 128, 16, dtype)
+    g = W.generator(95 + int(q_sigma))
+    case = dataclasses.replace(case, q=W.normal(g, tuple(case.q.shape), q_sigma, dtype))
+    for causal in (True, False):
+        assert_close(run(case, causal), case.oracle(causal), what=f"peaked {dtype} q_sigma {q_sigma} causal {causal}")
