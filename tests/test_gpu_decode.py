@@ -200,3 +200,55 @@ def test_sliding_window_long_sequence_split():
     got = P.attn_decode(c.q, c.k_cache, c.v_cache, c.tables, c.lens, c.scale, window=4097)
     torch.cuda.synchronize()
     assert_close(got, oracle_window(case, 4097), what="window 4097")
+
+
+def test_decode_sees_inputs_rewritten_by_another_kernel_just_before_it():
+    """Every kernel of the library is a programmatic dependent of the work before
+    it on the stream and waits for that grid before reading: tables, lengths,
+    queries and a cache row rewritten by another library's kernels immediately
+    before the call are seen -- eagerly and inside a captured graph."""
+    import dataclasses
+    case = decode_case(71, [300, 17, 1000, 64], 32, 8, 128, 16)
+    # the last token of sequence 2 gets new K/V values (written by a torch kernel)
+    g = W.generator(72)
+    k_new = W.normal(g, (8, 128), 1.0, "f16")
+    v_new = W.normal(g, (8, 128), 1.0, "f16")
+    L = int(case.lens[2])
+    phys, off = int(case.tables[2, (L - 1) // 16]), (L - 1) % 16
+    kc, vc = case.k_cache.clone(), case.v_cache.clone()
+    kc[phys, off] = k_new
+    vc[phys, off] = v_new
+    want = dataclasses.replace(case, k_cache=kc, v_cache=vc).oracle()
+
+    c = case.to("cuda")
+    src = dict(tables=c.tables.clone(), lens=c.lens.clone(), q=c.q.clone(), k=k_new.cuda(), v=v_new.cuda())
+    dst = dict(tables=torch.zeros_like(c.tables), lens=torch.ones_like(c.lens), q=torch.zeros_like(c.q))
+    out = torch.empty(c.q.shape, dtype=torch.float32, device="cuda")
+    ws = torch.empty(P.decode_workspace_size(4, 32, 8, 128), dtype=torch.uint8, device="cuda")
+
+    def step():
+        # elementwise kernels (not copies) write every input of the call
+        for name in ("tables", "lens", "q"):
+            torch.mul(src[name], 1, out=dst[name])
+        torch.mul(src["k"], 1, out=c.k_cache[phys, off])
+        torch.mul(src["v"], 1, out=c.v_cache[phys, off])
+        P.attn_decode(dst["q"], c.k_cache, c.v_cache, dst["tables"], dst["lens"], c.scale, out=out, workspace=ws)
+
+    def scramble():
+        for t in dst.values():
+            t.zero_()
+        c.k_cache[phys, off].zero_()
+        c.v_cache[phys, off].zero_()
+
+    for _ in range(3):
+        scramble()
+        step()
+        torch.cuda.synchronize()
+        assert_close(out, want, what="eager")
+    graph = P.StepGraph(step)
+    for _ in range(3):
+        scramble()
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_close(out, want, what="graph")
