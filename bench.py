@@ -334,15 +334,18 @@ def time_device_graph(step: DecodeStep, steps: int, warmup: int, barrier):
     for _ in range(warmup):
         graph.replay()
     torch.cuda.synchronize()
-    # per-launch decode time for the roofline, from eager calls of layer 0
-    # (they are device-bound; the graph would hide the split between kernels)
-    a = [torch.cuda.Event(enable_timing=True) for _ in range(21)]
-    for i in range(20):
+    # per-launch decode time for the roofline: the decode call of every layer
+    # (distinct pools: together larger than L2 for every workload here)
+    # captured as one graph, so no host work sits between the launches
+    n_dec = max(layers, 4)
+    dec_graph = P.StepGraph(lambda: [step.decode(i % layers) for i in range(n_dec)])
+    a = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for i in range(5):
         a[i].record()
-        step.decode(0)
-    a[20].record()
+        dec_graph.replay()
+    a[5].record()
     torch.cuda.synchronize()
-    dec_eager = [a[i].elapsed_time(a[i + 1]) for i in range(20)]
+    dec_eager = [a[i].elapsed_time(a[i + 1]) / n_dec for i in range(5)]
     barrier()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
