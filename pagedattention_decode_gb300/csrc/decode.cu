@@ -170,16 +170,29 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
     float *sscale = reinterpret_cast<float *>(empty + NS);  // int8: [NS][2][hkv] per-stage block scales
     const int hg = blockIdx.y;
     const bool meta_cta = blockIdx.x == 0 && blockIdx.y == 0;
+    if (threadIdx.x == 0) {  // descriptors are kernel parameters: no wait needed
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+    }
     pdl_wait();  // the previous kernel on the stream (e.g. the slot write) is complete
 
     // ---- 1. total sub-blocks, this CTA's range ------------------------------
+    if (tid == 0) {
+        s_first_seq = -1;
+        s_abort = 0;
+    }
     int64_t total = 0;
+    int my_n = 0, my_incl = 0;  // this thread's sequence when they all fit one pass
     for (int s0 = 0; s0 < p.num_seqs; s0 += blockDim.x) {
         const int s = s0 + tid;
         const int n = s < p.num_seqs ? decode_sub_blocks(p, s) : 0;
         if (meta_cta && s < p.num_seqs && decode_bad_length(p, s)) set_err(p.err, PKV_DEVERR_LENGTH);
         int chunk;
-        block_scan(n, s_warp, &chunk);
+        const int incl = block_scan(n, s_warp, &chunk);
+        if (s0 == 0) {
+            my_n = n;
+            my_incl = incl;
+        }
         total += chunk;
     }
     const int64_t want = (total + kMinSubBlocksPerCta - 1) / kMinSubBlocksPerCta;
@@ -188,23 +201,31 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
     const int64_t lo = ctas ? (int64_t)blockIdx.x * total / ctas : 0;
     const int64_t hi = ctas ? (int64_t)(blockIdx.x + 1) * total / ctas : 0;
 
-    if (tid == 0) {
-        s_first_seq = -1;
-        s_abort = 0;
-    }
-    int64_t carry = 0;
-    for (int s0 = 0; s0 < p.num_seqs; s0 += blockDim.x) {
-        const int s = s0 + tid;
-        const int n = s < p.num_seqs ? decode_sub_blocks(p, s) : 0;
-        int chunk;
-        const int incl = block_scan(n, s_warp, &chunk);
-        const int64_t start = carry + incl - n;
-        if (n > 0 && start <= lo && lo < start + n) {
-            s_first_seq = s;
+    if (p.num_seqs <= (int)blockDim.x) {
+        // one pass held every sequence: its prefix sums locate the range start
+        // (ordered after s_first_seq = -1 by the scan's barriers; read after
+        // the barrier below)
+        const int64_t start = my_incl - my_n;
+        if (my_n > 0 && start <= lo && lo < start + my_n) {
+            s_first_seq = tid;
             s_first_start = (int)start;
         }
-        if (meta_cta && s < p.num_seqs) p.ws_meta[2 + s] = (int)start;
-        carry += chunk;
+        if (meta_cta && tid < p.num_seqs) p.ws_meta[2 + tid] = (int)start;
+    } else {
+        int64_t carry = 0;
+        for (int s0 = 0; s0 < p.num_seqs; s0 += blockDim.x) {
+            const int s = s0 + tid;
+            const int n = s < p.num_seqs ? decode_sub_blocks(p, s) : 0;
+            int chunk;
+            const int incl = block_scan(n, s_warp, &chunk);
+            const int64_t start = carry + incl - n;
+            if (n > 0 && start <= lo && lo < start + n) {
+                s_first_seq = s;
+                s_first_start = (int)start;
+            }
+            if (meta_cta && s < p.num_seqs) p.ws_meta[2 + s] = (int)start;
+            carry += chunk;
+        }
     }
     if (meta_cta && tid == 0) {
         p.ws_meta[0] = (int)total;
@@ -226,10 +247,6 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
     // Both roles walk the same list; `x` counts concatenated sub-blocks.
     if (warp == 0) {
         // ===== producer =====
-        if (lane == 0) {
-            prefetch_tensormap(&tmk);
-            prefetch_tensormap(&tmv);
-        }
         const uint64_t pol = policy_evict_first();
         int it = 0;
         bool aborted = false;
