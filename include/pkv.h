@@ -29,6 +29,11 @@
  *  - Device calls are asynchronous on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream).  Argument checks that need no device data are
  *    done on the host before any launch; a failing check launches nothing.
+ *    Kernels are launched as programmatic dependents of the work before them
+ *    on the stream and wait for that grid (complete, memory visible) before
+ *    touching device memory, so inputs written by any earlier kernel on the
+ *    stream are seen.  No call synchronises the host or allocates, so a step
+ *    of calls can be captured in a CUDA graph.
  *  - `err_word` (optional, may be NULL) is a device int32 the kernels OR bits
  *    into (PKV_DEVERR_*) when they meet bad device-side data (a slot or block
  *    id outside the pool, a wait that ran out).  The offending item is
@@ -197,8 +202,9 @@ PKV_API pkv_status pkv_attn_decode_noalloc(const void *q, int64_t q_token_stride
  * rows and kv_len = seq_lens[s] keys (the new rows' keys already written),
  * attends keys t <= kv_len - q_len + i when causal != 0, else all kv_len keys.
  * Rows with q_len == 1 take the split-K decode path; longer chunks run on the
- * tcgen05 tensor cores (accumulators in tensor memory).  q_len > kv_len sets
- * PKV_DEVERR_LENGTH and skips the sequence.
+ * tcgen05 tensor cores (accumulators in tensor memory), with the softmax
+ * weights entering P V as fp16 (an fp16 cache) or as a bf16 hi + lo pair (a
+ * bf16 cache).  q_len > kv_len sets PKV_DEVERR_LENGTH and skips the sequence.
  *
  *   q             device [total_q, num_q_heads, head_dim], row r at r * q_token_stride;
  *                 when max_q_len > 1, q and its row stride must be 16-byte aligned.
