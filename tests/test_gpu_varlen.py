@@ -96,3 +96,16 @@ def test_peaked_attention_prefill(dtype, q_sigma):
     case = dataclasses.replace(case, q=W.normal(g, tuple(case.q.shape), q_sigma, dtype))
     for causal in (True, False):
         assert_close(run(case, causal), case.oracle(causal), what=f"peaked {dtype} q_sigma {q_sigma} causal {causal}")
+
+
+@pytest.mark.parametrize("bs", [64, 128, 256])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_large_blocks_use_tall_tma_boxes(bs, dtype):
+    """The prefill kernel loads K/V with the tallest TMA box (16, 32, 64 or 128
+    rows) that divides block_size; blocks of 64-256 tokens take the 64- and
+    128-row boxes, with ragged sequence tails inside a box."""
+    q_lens = [300, 1, 77, 129]
+    kv_lens = [300 + 500, 700, 77, 129 + 64]
+    case = varlen_case(110 + bs, q_lens, kv_lens, 32, 8, 128, bs, dtype, sigma=1.0 if dtype == "f16" else 0.5)
+    for causal in (True, False):
+        assert_close(run(case, causal), case.oracle(causal), what=f"bs {bs} {dtype} causal {causal}")
