@@ -289,6 +289,15 @@ class DecodeStepInt8(DecodeStep):
         return dec, wr
 
 
+def max_over_ranks(x: float, pg, dev) -> float:
+    """The slowest rank's value (the job takes as long as its slowest replica)."""
+    if pg is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
 def time_device(step: DecodeStep, steps: int, warmup: int, barrier):
     stream = torch.cuda.current_stream()
     layers = step.w.layers
@@ -540,10 +549,10 @@ def reference_arm(args, rank: int):
         return
     w = W.gqa_decode()
     total = args.steps + args.warmup
-    # size each step so the whole run stays near a minute of CPU time
-    rate, n1, dt1, cores = oracle_sample_rate(w, 0.5)
+    # size each step so the whole run stays near --ref-seconds of CPU time
+    rate, n1, dt1, cores = oracle_sample_rate(w, min(0.5, args.ref_seconds))
     per_seq = dt1 / n1
-    n = max(1, min(w.batch, int(60.0 / max(total, 1) / per_seq)))
+    n = max(1, min(w.batch, int(args.ref_seconds / max(total, 1) / per_seq)))
     for _ in range(args.warmup):
         oracle_sample_rate(w, 0, seqs_per_call=n)
     times, gbs = [], []
@@ -741,6 +750,8 @@ def main():
                     help="gqa: the headline decode step (GQA 32/8, B 256); gqa_int8: the same over an int8 "
                          "cache; gpt2: 12-layer MHA decode step; "
                          "skew: long/skewed split-K decode; mixed: the packed prefill+decode step")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="reference arm: CPU seconds the whole --steps/--warmup run is sized to")
     ap.add_argument("--batch", type=int, default=0,
                     help="use only the first N sequences (a smaller case of the same workload, for profiling)")
     args = ap.parse_args()
@@ -783,10 +794,7 @@ def main():
     total_ms, dec_ms, wr_ms, clocks = timer(step, args.steps, args.warmup, barrier)
     dec_b, wr_b = step.bytes()
     step_bytes = (dec_b + wr_b) * w.layers
-    if pg is not None:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, pg, dev)
     ms_per_step = total_ms / args.steps
     value = world * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
     tokens_per_s = world * w.batch * args.steps / (total_ms * 1e-3)  # one new token per sequence per step (all layers)
@@ -833,6 +841,7 @@ def main():
         n_e2e = max(1, min(args.steps, 200))
         ser_ms, _, _, _ = time_e2e(w, step, n_e2e, 3, barrier, pipelined=False)
         e2e_ms, e2e_bytes, h2d, d2h = time_e2e(w, step, n_e2e, 3, barrier)
+        e2e_ms, ser_ms = max_over_ranks(e2e_ms, pg, dev), max_over_ranks(ser_ms, pg, dev)
         line["e2e"] = {"value": world * e2e_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / n_e2e, "steps": n_e2e,
                        "tokens_per_s": world * w.batch * n_e2e / (e2e_ms * 1e-3),
