@@ -119,6 +119,15 @@ __device__ __forceinline__ int block_scan(int v, int *warp_sums, int *total) {
 // 1024 + u exactly, minus 1152 = the signed code.  bf16: through binary32
 // (2^23 + u, minus 2^23 + 128), then an exact narrowing.
 template <typename T>
+struct IsHalf {
+    static constexpr bool value = false;
+};
+template <>
+struct IsHalf<__half> {
+    static constexpr bool value = true;
+};
+
+template <typename T>
 __device__ __forceinline__ uint32_t i8_pair(uint32_t x, uint32_t sel);
 
 template <>
@@ -126,6 +135,13 @@ __device__ __forceinline__ uint32_t i8_pair<__half>(uint32_t x, uint32_t sel) {
     uint32_t h = __byte_perm(x, 0x64646464u, sel);
     __half2 v = __hsub2(*reinterpret_cast<__half2 *>(&h), __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// fp16 codes + 1152 (1024 + 128 + code, exact) without the subtraction: the
+// decode kernel takes the bias out of the scores (1152 * sum of q) and out of
+// O (1152 * sum of the P fed to the MMA) instead.
+__device__ __forceinline__ uint32_t i8_pair_biased(uint32_t x, uint32_t sel) {
+    return __byte_perm(x, 0x64646464u, sel);
 }
 
 template <>
@@ -373,6 +389,22 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
             }
         }
         float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+        // int8 codes of an fp16 cache enter the MMAs as code + 1152 (see i8_pair_biased)
+        constexpr bool BIAS = I8 && IsHalf<T>::value;
+        float qsA = 0.f, qsB = 0.f, pvA = 0.f, pvB = 0.f;
+        if constexpr (BIAS) {
+            // sum of q over head_dim for heads hA, hB: lane 4g + t4 holds a quarter of head g
+            float qs = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const float2 a = unpack2<T>(qf[kk][0]), b = unpack2<T>(qf[kk][1]);
+                qs += (a.x + a.y) + (b.x + b.y);
+            }
+            qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+            qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+            qsA = __shfl_sync(0xffffffffu, qs, hA * 4);
+            qsB = __shfl_sync(0xffffffffu, qs, hB * 4);
+        }
         float o[D / 16][4];
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -407,8 +439,18 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const uint32_t lo = r[2 * u] ^ 0x80808080u, hi = r[2 * u + 1] ^ 0x80808080u;
-                        const uint32_t a[4] = {i8_pair<T>(lo, 0x4140u), i8_pair<T>(hi, 0x4140u),
-                                               i8_pair<T>(lo, 0x4342u), i8_pair<T>(hi, 0x4342u)};
+                        uint32_t a[4];
+                        if constexpr (BIAS) {
+                            a[0] = i8_pair_biased(lo, 0x4140u);
+                            a[1] = i8_pair_biased(hi, 0x4140u);
+                            a[2] = i8_pair_biased(lo, 0x4342u);
+                            a[3] = i8_pair_biased(hi, 0x4342u);
+                        } else {
+                            a[0] = i8_pair<T>(lo, 0x4140u);
+                            a[1] = i8_pair<T>(hi, 0x4140u);
+                            a[2] = i8_pair<T>(lo, 0x4342u);
+                            a[3] = i8_pair<T>(hi, 0x4342u);
+                        }
                         mma_16816<T>(sc, a, qf[2 * k2 + u][0], qf[2 * k2 + u][1]);
                     }
                 }
@@ -422,7 +464,19 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
                     mma_16816<T>(sc, a, qf[kk][0], qf[kk][1]);
                 }
             }
-            float x0 = sc[0] * ssl, x1 = sc[1] * ssl, x2 = sc[2] * ssl, x3 = sc[3] * ssl;
+            float x0, x1, x2, x3;
+            if constexpr (BIAS) {
+                const float kA = 1152.f * qsA * ssl, kB = 1152.f * qsB * ssl;
+                x0 = fmaf(sc[0], ssl, -kA);
+                x1 = fmaf(sc[1], ssl, -kB);
+                x2 = fmaf(sc[2], ssl, -kA);
+                x3 = fmaf(sc[3], ssl, -kB);
+            } else {
+                x0 = sc[0] * ssl;
+                x1 = sc[1] * ssl;
+                x2 = sc[2] * ssl;
+                x3 = sc[3] * ssl;
+            }
             if (nv < kSub) {
                 if (g >= nv) x0 = x1 = -INFINITY;
                 if (g + 8 >= nv) x2 = x3 = -INFINITY;
@@ -457,6 +511,10 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
             // P as the B operand (16 tokens x 8 heads), hi and lo 16-bit parts
             // (int8: P is scaled by the block's V scale, so the codes multiply directly)
             const float q0 = p0 * vsc, q1 = p1 * vsc, q2 = p2 * vsc, q3 = p3 * vsc;
+            if constexpr (BIAS) {  // the P fed to P V, per head, rescaled as O is
+                pvA = pvA * aA + (q0 + q2);
+                pvB = pvB * aB + (q1 + q3);
+            }
             const uint32_t h01 = pack2<T>(q0, q1), h23 = pack2<T>(q2, q3);
             const float2 r01 = unpack2<T>(h01), r23 = unpack2<T>(h23);
             const uint32_t l01 = pack2<T>(q0 - r01.x, q1 - r01.y), l23 = pack2<T>(q2 - r23.x, q3 - r23.y);
@@ -480,8 +538,18 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const uint32_t lo = r[2 * u] ^ 0x80808080u, hi = r[2 * u + 1] ^ 0x80808080u;
-                        const uint32_t a[4] = {i8_pair<T>(lo, 0x4240u), i8_pair<T>(lo, 0x4341u),
-                                               i8_pair<T>(hi, 0x4240u), i8_pair<T>(hi, 0x4341u)};
+                        uint32_t a[4];
+                        if constexpr (BIAS) {
+                            a[0] = i8_pair_biased(lo, 0x4240u);
+                            a[1] = i8_pair_biased(lo, 0x4341u);
+                            a[2] = i8_pair_biased(hi, 0x4240u);
+                            a[3] = i8_pair_biased(hi, 0x4341u);
+                        } else {
+                            a[0] = i8_pair<T>(lo, 0x4240u);
+                            a[1] = i8_pair<T>(lo, 0x4341u);
+                            a[2] = i8_pair<T>(hi, 0x4240u);
+                            a[3] = i8_pair<T>(hi, 0x4341u);
+                        }
                         mma_16816<T>(o[2 * m2 + u], a, bh0, bh1);
                         mma_16816<T>(o[2 * m2 + u], a, bl0, bl1);
                     }
@@ -516,6 +584,21 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
         for (int off = 4; off < 32; off <<= 1) {
             lA += __shfl_xor_sync(0xffffffffu, lA, off);
             lB += __shfl_xor_sync(0xffffffffu, lB, off);
+        }
+        if constexpr (BIAS) {
+            // O holds sum_t P_t (code_t + 1152): take 1152 * sum_t P_t out
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                pvA += __shfl_xor_sync(0xffffffffu, pvA, off);
+                pvB += __shfl_xor_sync(0xffffffffu, pvB, off);
+            }
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                o[mt][0] = fmaf(-1152.f, pvA, o[mt][0]);
+                o[mt][2] = fmaf(-1152.f, pvA, o[mt][2]);
+                o[mt][1] = fmaf(-1152.f, pvB, o[mt][1]);
+                o[mt][3] = fmaf(-1152.f, pvB, o[mt][3]);
+            }
         }
         const bool complete = (sb == 0 && b1 == n_s);
         if (complete) {
