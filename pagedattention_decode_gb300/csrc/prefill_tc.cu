@@ -88,23 +88,30 @@ __host__ __device__ constexpr uint32_t idesc_f16(int bf16, int b_mn_major, int M
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The MMA and commit wrappers are executed by a whole, converged warp: the
+// warp computes the (uniform) operands and one lane elected inside the
+// instruction sequence issues it.  Issuing from a single-lane branch instead
+// costs more per MMA than the MMA itself takes on the tensor pipe.
 __device__ __forceinline__ void umma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
         "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
 __device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
 }
 
+// Arrives once on `bar` when every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -138,6 +145,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
             taddr),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
         "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
+}
+
+// max(a, b, c) in one instruction (three-input form of max.f32 on sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -336,8 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(&v_full[k % S], (k / S) & 1, &never);
         }
     } else if (warp == 1) {
-        // ===== MMA issuer =====
-        if (lane == 0) {
+        // ===== MMA issuer: the whole warp walks the loop, one elected lane issues =====
+        {
+            // every lane waits on the same phase; the vote keeps the warp converged
+            auto wait = [&](uint64_t *bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, &s_abort));
+            };
             const uint32_t idS = idesc_f16(BF ? 1 : 0, 0, 128, kTok);
             const uint32_t idPV = idesc_f16(BF ? 1 : 0, 1, 128, D);
             const uint32_t sq_a = smem_u32(sq), sk_a = smem_u32(sk), sv_a = smem_u32(sv);
@@ -364,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 umma_commit(o_done(u));
             };
-            bool ok = mbar_wait(q_full, 0, &s_abort) && mbar_wait(&k_full[0], 0, &s_abort);
+            bool ok = wait(q_full, 0) && wait(&k_full[0], 0);
             if (ok) {
                 tc_fence_after();
                 for (int u = 0; u < kTiles; ++u)
@@ -377,17 +395,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool v_ready = false, k_ready = false;
                 for (int u = 0; u < kTiles && ok; ++u) {
                     if (j >= steps_of(u)) continue;
-                    ok = mbar_wait(p_full(u), ph, &s_abort);
+                    ok = wait(p_full(u), ph);
                     // the last step's V rows past kv_len are cleared by tile zt
-                    if (ok && u != zt && (j_first + j + 1) * kTok > kv_len) ok = mbar_wait(p_full(zt), ph, &s_abort);
-                    if (ok && !v_ready) ok = v_ready = mbar_wait(&v_full[j % S], (j / S) & 1, &s_abort);
+                    if (ok && u != zt && (j_first + j + 1) * kTok > kv_len) ok = wait(p_full(zt), ph);
+                    if (ok && !v_ready) ok = v_ready = wait(&v_full[j % S], (j / S) & 1);
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv(u, j);
                     if (j1 < steps_of(u)) {
-                        if (!k_ready) ok = k_ready = mbar_wait(&k_full[j1 % S], (j1 / S) & 1, &s_abort);
+                        if (!k_ready) ok = k_ready = wait(&k_full[j1 % S], (j1 / S) & 1);
                         // the scores overwrite P of step j: its P V must have completed
-                        if (ok) ok = mbar_wait(o_done(u), ph, &s_abort);
+                        if (ok) ok = wait(o_done(u), ph);
                         if (!ok) break;
                         tc_fence_after();
                         issue_s(u, j1);
@@ -397,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(&v_empty[j % S]);
                 if (k_ready) umma_commit(&k_empty[j1 % S]);
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 s_abort = 1;
                 set_err(p.err, PKV_DEVERR_TIMEOUT);
             }
@@ -445,14 +463,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(key <= lim && key >= lo)) sr[c] = __float_as_uint(-INFINITY);
                 }
             }
-            // the row max of the raw scores (the scale is positive)
+            // the row max of the raw scores (the scale is positive): eight
+            // independent chains of three-input maxima
             float pm[8];
 #pragma unroll
-            for (int v = 0; v < 8; ++v) pm[v] = -INFINITY;
+            for (int v = 0; v < 8; ++v) pm[v] = fmaxf(__uint_as_float(sr[v]), __uint_as_float(sr[8 + v]));
 #pragma unroll
-            for (int c = 0; c < kTok; ++c) pm[c & 7] = fmaxf(pm[c & 7], __uint_as_float(sr[c]));
-            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * sl;
+            for (int c = 16; c < kTok; c += 16)
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    pm[v] = fmax3(pm[v], __uint_as_float(sr[c + v]), __uint_as_float(sr[c + 8 + v]));
+            const float mx =
+                fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7]))) * sl;
             const float m_new = fmaxf(m_used, mx);
             const bool need = m_new > m_used + kRescaleLog2;
             const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
@@ -471,26 +493,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lsum *= alpha;
                 m_used = m_new;
             }
-            // p = 2^(s * scale - m), written back as 16-bit values.  With a
-            // window a row can meet whole tiles before its first key: there
-            // m_used is still -inf and those p must be 0, not NaN.
-            const bool none_yet = m_used == -INFINITY;
-            const float neg_m = -m_used;
-            float ps[8];
+            // p = 2^(s * scale - m), written back as 16-bit values; the scale
+            // and shift, and the row sum, as packed fp32 pairs.  With a window
+            // a row can meet whole tiles before its first key: there every
+            // score is -inf and m_used is still -inf, so the shift is taken as
+            // -inf too and every p comes out 0 (not NaN).
+            const float neg_m = m_used == -INFINITY ? -INFINITY : -m_used;
+            const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(neg_m, neg_m);
+            float2 ps[4];
 #pragma unroll
-            for (int v = 0; v < 8; ++v) ps[v] = 0.f;
+            for (int v = 0; v < 4; ++v) ps[v] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c0 = 0; c0 < kTok; c0 += 32) {
                 uint32_t ph[16], pl[16];
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
-                    float p0 = fast_exp2(fmaf(__uint_as_float(sr[c0 + c]), sl, neg_m));
-                    float p1 = fast_exp2(fmaf(__uint_as_float(sr[c0 + c + 1]), sl, neg_m));
-                    if (none_yet) {
-                        p0 = 0.f;
-                        p1 = 0.f;
-                    }
-                    ps[(c >> 1) & 7] += p0 + p1;
+                    const float2 x =
+                        __ffma2_rn(make_float2(__uint_as_float(sr[c0 + c]), __uint_as_float(sr[c0 + c + 1])), sl2, nm2);
+                    const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                    ps[(c >> 1) & 3] = __fadd2_rn(ps[(c >> 1) & 3], make_float2(p0, p1));
                     const uint32_t h = pack2<T>(p0, p1);
                     ph[c / 2] = h;
                     if (LO) {
@@ -505,7 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st16(trow_addr + c0 / 2, ph);
                 }
             }
-            lsum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+            const float2 ps01 = __fadd2_rn(ps[0], ps[1]), ps23 = __fadd2_rn(ps[2], ps[3]);
+            const float2 ps4 = __fadd2_rn(ps01, ps23);
+            lsum += ps4.x + ps4.y;
             // V rows past kv_len in the last tile hold stale or unrelated data: zero them
             if (u == zt && t0 + kTok > kv_len) {
                 if (row >= kv_len - t0) {
@@ -561,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- teardown ----
     tc_fence_before();
     __syncthreads();
-    if (s_abort && warp == 1 && lane == 0) {
+    if (warp == 1 && __all_sync(0xffffffffu, s_abort != 0)) {
         // an abandoned pipeline: let every MMA issued so far land before TMEM is released
         umma_commit(fin);
         volatile int never = 0;
