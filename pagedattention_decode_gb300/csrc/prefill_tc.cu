@@ -28,8 +28,10 @@
 //    TMEM loads, apply the causal and window limits, keep the
 //    running max and sum in registers, and write P back over the scores as
 //    16-bit values (bf16: a hi + lo pair, ~16 significant bits).  The running
-//    max is only moved when it grows by more than 2^8; then that row of O is
-//    rescaled in TMEM.  The final O row is divided by the sum and stored.
+//    max comes from the row's first tile with a visible key and is moved only
+//    when a step's p could pass 2^15 (their sum tells, so no per-step max is
+//    taken): then that row of O is rescaled in TMEM and P written again.  The
+//    final O row is divided by the sum and stored.
 // One CTA per SM: all 512 TMEM columns (per tile: S/P 128, O head_dim) and
 // ~197 KB of shared memory; setmaxnreg moves registers from the producer /
 // MMA warpgroup (warps 0-3) to the two softmax warpgroups.
@@ -45,7 +47,7 @@ namespace {
 constexpr int kTok = 128;         // keys per step: the N of the score MMA
 constexpr int kTiles = 2;         // q tiles of 128 M rows per CTA; every K/V stage serves both
 constexpr int kTmemCols = 512;    // 256 columns per tile: scores / P at +0 (128), O at +128 (D)
-constexpr float kRescaleLog2 = 8.f;
+constexpr float kPSumMax = 32768.f;  // a step's sum of p above this moves the running max
 
 template <typename T>
 struct IsBf16 {
@@ -154,6 +156,25 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
+// Non-blocking test of an mbarrier phase.  A phase that has completed is
+// seen at a fraction of the cost of the suspending wait, so every wait of
+// this kernel tests first and suspends only when the phase is still open.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    return mbar_test(bar, parity) || mbar_wait(bar, parity, abort);
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -185,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int KVSTAGE = HALVES * KVHALF;     // one K (or V) tile
     constexpr bool BF = IsBf16<T>::value;
     // P enters P V as a 16-bit operand.  fp16 keeps 11 significant bits of each
-    // p in [0, 2^8] (relative error <= 2^-12, far inside the 2e-3 gate); bf16
+    // p in [0, 2^15] (relative error <= 2^-12, far inside the 2e-3 gate); bf16
     // keeps only 8, so there P is split into hi + lo halves and P V takes two
     // MMAs per K step.  P of keys 32c .. 32c + 31 lies in TMEM columns
     // 16c .. 16c + 15 (fp16), or hi in 32c .. 32c + 15 and lo in 32c + 16 ..
@@ -325,13 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t dst_off = (uint32_t)(stage * KVSTAGE + (lane % HALVES) * KVHALF + (lane / HALVES) * box * 128);
             int okw = 1;
-            if (lane == 0) okw = mbar_wait(&k_empty[stage], ((j / S) & 1) ^ 1, &s_abort);
+            if (lane == 0) okw = wait_phase(&k_empty[stage], ((j / S) & 1) ^ 1, &s_abort);
             if (!__shfl_sync(0xffffffffu, okw, 0)) break;
             if (lane == 0) mbar_arrive_expect_tx(&k_full[stage], (uint32_t)(nbox * box * 128));
             __syncwarp();
             if (lane < nbox) tma_load_3d(sk + dst_off, &tmk, &k_full[stage], 0, kvh * HALVES + lane % HALVES, row, pol_kv);
             issued_k = j + 1;
-            if (lane == 0) okw = mbar_wait(&v_empty[stage], ((j / S) & 1) ^ 1, &s_abort);
+            if (lane == 0) okw = wait_phase(&v_empty[stage], ((j / S) & 1) ^ 1, &s_abort);
             if (!__shfl_sync(0xffffffffu, okw, 0)) break;
             if (lane == 0) mbar_arrive_expect_tx(&v_full[stage], (uint32_t)(nbox * box * 128));
             __syncwarp();
@@ -354,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
             // every lane waits on the same phase; the vote keeps the warp converged
             auto wait = [&](uint64_t *bar, uint32_t parity) {
-                return __all_sync(0xffffffffu, mbar_wait(bar, parity, &s_abort));
+                return __all_sync(0xffffffffu, wait_phase(bar, parity, &s_abort));
             };
             const uint32_t idS = idesc_f16(BF ? 1 : 0, 0, 128, kTok);
             const uint32_t idPV = idesc_f16(BF ? 1 : 0, 1, 128, D);
@@ -439,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int j = 0; j < ntu; ++j) {
             // warp-uniform outcome: the tcgen05 ld/st below are warp-collective
-            if (!__all_sync(0xffffffffu, mbar_wait(s_full(u), j & 1, &s_abort))) {
+            if (!__all_sync(0xffffffffu, wait_phase(s_full(u), j & 1, &s_abort))) {
                 ok = false;
                 break;
             }
@@ -463,74 +484,98 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(key <= lim && key >= lo)) sr[c] = __float_as_uint(-INFINITY);
                 }
             }
-            // the row max of the raw scores (the scale is positive): eight
+            // the row max of the raw scores times the scale (positive): eight
             // independent chains of three-input maxima
-            float pm[8];
+            auto row_max = [&]() -> float {
+                float pm[8];
 #pragma unroll
-            for (int v = 0; v < 8; ++v) pm[v] = fmaxf(__uint_as_float(sr[v]), __uint_as_float(sr[8 + v]));
+                for (int v = 0; v < 8; ++v) pm[v] = fmaxf(__uint_as_float(sr[v]), __uint_as_float(sr[8 + v]));
 #pragma unroll
-            for (int c = 16; c < kTok; c += 16)
+                for (int c = 16; c < kTok; c += 16)
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    pm[v] = fmax3(pm[v], __uint_as_float(sr[c + v]), __uint_as_float(sr[c + 8 + v]));
-            const float mx =
-                fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7]))) * sl;
-            const float m_new = fmaxf(m_used, mx);
-            const bool need = m_new > m_used + kRescaleLog2;
-            const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
-            if (__any_sync(0xffffffffu, need) && j > 0) {
+                    for (int v = 0; v < 8; ++v)
+                        pm[v] = fmax3(pm[v], __uint_as_float(sr[c + v]), __uint_as_float(sr[c + 8 + v]));
+                return fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7]))) * sl;
+            };
+            // The running max m_used is taken from the row's first tile with
+            // a visible key and is moved only when p would leave the range
+            // where it is exact enough and finite as a 16-bit value: every p of
+            // a step is at most the step's sum, so a sum <= 2^15 proves all p
+            // <= 2^15.  Otherwise (or on inf / NaN) the row takes the exact
+            // max, O and the row sum are rescaled, and P is written again (a
+            // second pass of the loop below).
+            const bool fresh = m_used == -INFINITY;
+            if (__any_sync(0xffffffffu, fresh) && fresh) m_used = row_max();
+            float step_sum;
+#pragma unroll 1
+            for (int pass = 0;; ++pass) {
+                // p = 2^(s * scale - m_used), written back over the scores as
+                // 16-bit values (the scale and shift, and the row sum, as packed
+                // fp32 pairs).  While a row has met no key yet (a window can
+                // start past whole tiles) every score and m_used are -inf: the
+                // shift is then taken as -inf too, so every p is 0, not NaN.
+                const float neg_m = m_used == -INFINITY ? -INFINITY : -m_used;
+                const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(neg_m, neg_m);
+                float2 ps[4];
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t orr[32];
-                    tmem_ld32(trow_addr + 128 + c0, orr);
-                    tmem_wait_ld();
+                for (int v = 0; v < 4; ++v) ps[v] = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
-                    tmem_st32(trow_addr + 128 + c0, orr);
-                }
-            }
-            if (need) {
-                lsum *= alpha;
-                m_used = m_new;
-            }
-            // p = 2^(s * scale - m), written back as 16-bit values; the scale
-            // and shift, and the row sum, as packed fp32 pairs.  With a window
-            // a row can meet whole tiles before its first key: there every
-            // score is -inf and m_used is still -inf, so the shift is taken as
-            // -inf too and every p comes out 0 (not NaN).
-            const float neg_m = m_used == -INFINITY ? -INFINITY : -m_used;
-            const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(neg_m, neg_m);
-            float2 ps[4];
+                for (int c0 = 0; c0 < kTok; c0 += 32) {
+                    uint32_t ph[16], pl[16];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) ps[v] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int c0 = 0; c0 < kTok; c0 += 32) {
-                uint32_t ph[16], pl[16];
-#pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    const float2 x =
-                        __ffma2_rn(make_float2(__uint_as_float(sr[c0 + c]), __uint_as_float(sr[c0 + c + 1])), sl2, nm2);
-                    const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-                    ps[(c >> 1) & 3] = __fadd2_rn(ps[(c >> 1) & 3], make_float2(p0, p1));
-                    const uint32_t h = pack2<T>(p0, p1);
-                    ph[c / 2] = h;
+                    for (int c = 0; c < 32; c += 2) {
+                        const float2 x = __ffma2_rn(
+                            make_float2(__uint_as_float(sr[c0 + c]), __uint_as_float(sr[c0 + c + 1])), sl2, nm2);
+                        const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                        ps[(c >> 1) & 3] = __fadd2_rn(ps[(c >> 1) & 3], make_float2(p0, p1));
+                        const uint32_t h = pack2<T>(p0, p1);
+                        ph[c / 2] = h;
+                        if (LO) {
+                            const float2 hf = unpack2<T>(h);
+                            pl[c / 2] = pack2<T>(p0 - hf.x, p1 - hf.y);
+                        }
+                    }
                     if (LO) {
-                        const float2 hf = unpack2<T>(h);
-                        pl[c / 2] = pack2<T>(p0 - hf.x, p1 - hf.y);
+                        tmem_st16(trow_addr + c0, ph);
+                        tmem_st16(trow_addr + c0 + 16, pl);
+                    } else {
+                        tmem_st16(trow_addr + c0 / 2, ph);
                     }
                 }
-                if (LO) {
-                    tmem_st16(trow_addr + c0, ph);
-                    tmem_st16(trow_addr + c0 + 16, pl);
-                } else {
-                    tmem_st16(trow_addr + c0 / 2, ph);
+                const float2 ps01 = __fadd2_rn(ps[0], ps[1]), ps23 = __fadd2_rn(ps[2], ps[3]);
+                const float2 ps4 = __fadd2_rn(ps01, ps23);
+                step_sum = ps4.x + ps4.y;
+                const bool over = pass == 0 && !(step_sum <= kPSumMax);
+                if (!__any_sync(0xffffffffu, over)) break;
+                tmem_wait_st();
+                float alpha = 1.f;
+                if (over) {
+                    const float m_new = fmaxf(m_used, row_max());
+                    alpha = fast_exp2(m_used - m_new);
+                    lsum *= alpha;
+                    m_used = m_new;
+                }
+                if (j > 0) {
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t orr[32];
+                        tmem_ld32(trow_addr + 128 + c0, orr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
+                        tmem_st32(trow_addr + 128 + c0, orr);
+                    }
                 }
             }
-            const float2 ps01 = __fadd2_rn(ps[0], ps[1]), ps23 = __fadd2_rn(ps[2], ps[3]);
-            const float2 ps4 = __fadd2_rn(ps01, ps23);
-            lsum += ps4.x + ps4.y;
-            // V rows past kv_len in the last tile hold stale or unrelated data: zero them
+            lsum += step_sum;
+            // V rows past kv_len in the last tile hold stale or unrelated data:
+            // zero them, once the tile's TMA load (which may cover some of
+            // them) has landed
             if (u == zt && t0 + kTok > kv_len) {
+                if (!wait_phase(&v_full[j % S], (j / S) & 1, &s_abort)) {
+                    s_abort = 1;
+                    set_err(p.err, PKV_DEVERR_TIMEOUT);
+                }
                 if (row >= kv_len - t0) {
 #pragma unroll
                     for (int half = 0; half < HALVES; ++half) {
@@ -545,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(p_full(u));
         }
-        if (ok && ntu > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done(u), (ntu - 1) & 1, &s_abort));
+        if (ok && ntu > 0) ok = __all_sync(0xffffffffu, wait_phase(o_done(u), (ntu - 1) & 1, &s_abort));
         if (ok && ntu > 0) {
             tc_fence_after();
             const float inv = 1.f / lsum;
