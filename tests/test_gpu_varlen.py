@@ -98,6 +98,32 @@ def test_peaked_attention_prefill(dtype, q_sigma):
         assert_close(run(case, causal), case.oracle(causal), what=f"peaked {dtype} q_sigma {q_sigma} causal {causal}")
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("factor", [4.0, 8.0])
+def test_scores_jump_after_the_first_tiles(dtype, factor):
+    """The keys of the later half of every context are scaled up, so a row's
+    top scores rise by ~13 (factor 4) or ~30 (factor 8) log2 units after its
+    first tiles.  The prefill kernel takes its running max from a row's first
+    tile with a visible key: with factor 4 most rows keep that max and carry p
+    of up to ~2^13 as 16-bit operands; with factor 8 a step's p would pass
+    2^15, so the row moves its max, rescales O and its sum, and writes P
+    again."""
+    import dataclasses
+    q_lens = [300, 1, 129, 520]
+    kv_lens = [300 + 700, 900, 129 + 300, 520]
+    bs = 16
+    case = varlen_case(130 + int(factor), q_lens, kv_lens, 32, 8, 128, bs, dtype)
+    k = case.k_cache.clone()
+    for s, L in enumerate(kv_lens):
+        nblk = W.blocks_for(L, bs)
+        for j in range(nblk // 2, nblk):
+            phys = int(case.tables[s, j])
+            k[phys] = (k[phys].float() * factor).to(k.dtype)
+    case = dataclasses.replace(case, k_cache=k)
+    for causal in (True, False):
+        assert_close(run(case, causal), case.oracle(causal), what=f"jump x{factor} {dtype} causal {causal}")
+
+
 @pytest.mark.parametrize("bs", [64, 128, 256])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_large_blocks_use_tall_tma_boxes(bs, dtype):
