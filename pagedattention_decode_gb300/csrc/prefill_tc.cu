@@ -70,9 +70,10 @@ struct TcParams {
     void *out;
     int32_t out_f32;
     int32_t *err;
-    int32_t q_tiles;  // pairs of q tiles per sequence (kTiles * 128 / group positions each)
+    int32_t q_tiles;  // most pairs of q tiles in a sequence (kTiles * 128 / group positions each)
     int32_t window;   // > 0: each row attends only its most recent `window` keys
     int32_t box_rows; // rows per K/V TMA box: 128, 64, 32 or 16, a divisor of block_size
+    int32_t num_seqs;
 };
 
 // UMMA shared-memory descriptor, 128-byte swizzle (sm_100 family layout:
@@ -194,6 +195,14 @@ constexpr int kRegsLow = 72;
 constexpr int kRegsHigh = 216;
 constexpr int kRegsAtLaunchMin = (128 * kRegsLow + 256 * kRegsHigh + kThreads - 1) / kThreads;
 
+// A work item: the pair of q tiles `pair` (2 x 128 M rows) of KV head `kvh`
+// of the prefill chunk of sequence `s`.  The producer warp finds a CTA's
+// items and hands them to the other warps through a two-slot ring in shared
+// memory; nt0 < 0 marks the end.
+struct TcItem {
+    int s, kvh, q_begin, q_len, kv_len, q00, j_first, nt0, nt1;
+};
+
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -213,7 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 32c + 31 (bf16): columns whose scores have already been read.
     constexpr bool LO = BF;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bars[1 + 4 * S + 3 * kTiles + 1];
+    __shared__ uint64_t bars[2 + 4 * S + 3 * kTiles + 4 + 1];
+    __shared__ TcItem s_item[2];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -221,55 +231,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sk = base + kTiles * QTILE;
     uint8_t *sv = sk + S * KVSTAGE;
     uint64_t *q_full = &bars[0];
-    uint64_t *k_full = &bars[1];
-    uint64_t *k_empty = &bars[1 + S];
-    uint64_t *v_full = &bars[1 + 2 * S];
-    uint64_t *v_empty = &bars[1 + 3 * S];
-    uint64_t *tile_bars = &bars[1 + 4 * S];  // per tile: s_full, p_full, o_done
-    uint64_t *fin = &bars[1 + 4 * S + 3 * kTiles];  // abort path: completion of every MMA issued
+    uint64_t *q_empty = &bars[1];  // every score MMA of an item has read its Q
+    uint64_t *k_full = &bars[2];
+    uint64_t *k_empty = &bars[2 + S];
+    uint64_t *v_full = &bars[2 + 2 * S];
+    uint64_t *v_empty = &bars[2 + 3 * S];
+    uint64_t *tile_bars = &bars[2 + 4 * S];  // per tile: s_full, p_full, o_done
+    uint64_t *item_full = &bars[2 + 4 * S + 3 * kTiles];
+    uint64_t *item_empty = item_full + 2;
+    uint64_t *fin = item_full + 4;  // abort path: completion of every MMA issued
     auto s_full = [&](int u) { return tile_bars + u * 3; };
     auto p_full = [&](int u) { return tile_bars + u * 3 + 1; };
     auto o_done = [&](int u) { return tile_bars + u * 3 + 2; };
 
     pdl_wait();  // the previous kernel on the stream (e.g. the slot write) is complete
     pdl_trigger();
-    const int s = blockIdx.y;
-    const int kvh = blockIdx.z;
-    const int pair = p.q_tiles - 1 - blockIdx.x;  // longest causal tiles first
-    const int q_begin = p.cu_q[s];
-    const int q_len = p.cu_q[s + 1] - q_begin;
-    const int kv_len = p.seq_lens[s];
     const int G = p.group;
-    const int R = 128 / G;                        // query positions per tile
-    if (q_len <= 1 || pair * kTiles * R >= q_len) return;
-    if (q_len > kv_len || (int64_t)kv_len > (int64_t)p.max_blocks * p.block_size) {
-        if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0) set_err(p.err, PKV_DEVERR_LENGTH);
-        return;
-    }
-    // tile u holds positions q0(u) .. q0(u) + R - 1; the window's first key is
-    // lowest for the first row of tile 0, so both tiles walk from j_first
-    const int q00 = pair * kTiles * R;
-    const int lim_first = p.causal ? kv_len - q_len + q00 : kv_len - 1;
-    const int lo_first = (p.window > 0 && lim_first - p.window + 1 > 0) ? lim_first - p.window + 1 : 0;
-    const int j_first = lo_first / kTok;
-    auto tile_steps = [&](int u) -> int {
-        const int q0 = q00 + u * R;
-        if (q0 >= q_len) return 0;
-        const int last_row = min(q_len, q0 + R) - 1;
-        const int kv_hi = p.causal ? kv_len - q_len + last_row + 1 : kv_len;
-        return (kv_hi + kTok - 1) / kTok - j_first;
-    };
-    const int nt0 = tile_steps(0), nt1 = tile_steps(1);
-    const int nt = max(nt0, nt1);
-    auto steps_of = [&](int u) { return u ? nt1 : nt0; };
-    // V rows past kv_len (only in the last step) are cleared by the first tile
-    // whose P V reads that step
-    const int zt = nt0 == nt ? 0 : 1;
-
+    const int R = 128 / G;  // query positions per tile
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         s_abort = 0;
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int i = 0; i < S; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
@@ -280,6 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(s_full(u), 1);
             mbar_init(p_full(u), 128);
             mbar_init(o_done(u), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&item_full[i], 1);
+            mbar_init(&item_empty[i], 1 + 2 * 4);  // the MMA warp and the eight softmax warps
         }
         mbar_init(fin, 1);
         fence_barrier_init();
@@ -293,78 +280,184 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
+    // steps of tile u in an item, and the step count that both tiles walk
+    auto tile_steps = [&](const TcItem &it, int u) -> int {
+        const int q0 = it.q00 + u * R;
+        if (q0 >= it.q_len) return 0;
+        const int last_row = min(it.q_len, q0 + R) - 1;
+        const int kv_hi = p.causal ? it.kv_len - it.q_len + last_row + 1 : it.kv_len;
+        return (kv_hi + kTok - 1) / kTok - it.j_first;
+    };
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0) {
-        // ===== producer: Q of both tiles once, then K and V tiles =====
+        // ===== producer: finds the items, then Q of both tiles and the K and V tiles of each =====
         const uint64_t pol_q = policy_evict_first();
         const uint64_t pol_kv = policy_evict_last();  // re-read by the other q tiles of the chunk
-        const int ntiles = nt1 > 0 ? 2 : 1;
         if (lane == 0) {
             prefetch_tensormap(&tmq);
             prefetch_tensormap(&tmk);
             prefetch_tensormap(&tmv);
-            mbar_arrive_expect_tx(q_full, (uint32_t)(ntiles * G * HALVES * R * 128));
         }
-        __syncwarp();
-        for (int t = lane; t < ntiles * G * HALVES; t += 32) {
-            const int u = t / (G * HALVES), g = (t / HALVES) % G, half = t % HALVES;
-            tma_load_3d(sq + u * QTILE + half * QHALF + g * R * 128, &tmq, q_full, 0, (kvh * G + g) * HALVES + half,
-                        q_begin + q00 + u * R, pol_q);
-        }
-        const int32_t *trow = p.tables + (int64_t)s * p.max_blocks;
         const int box = p.box_rows;
-        // a tile has at most (128 / 16) * HALVES <= 16 boxes: lane t issues box t
-        // of K and of V (sub-block t / HALVES, half t % HALVES).  Its block-table
-        // entry is read one step ahead, off the issue path.
-        auto boxes_of = [&](int j) {
-            const int nvalid = min(kTok, kv_len - (j_first + j) * kTok);
-            return ((nvalid + box - 1) / box) * HALVES;
-        };
-        auto lookup = [&](int j) -> int {
-            if (j >= nt || lane >= boxes_of(j)) return 0;
-            const int tok = (j_first + j) * kTok + (lane / HALVES) * box;
-            return trow[tok / p.block_size];
-        };
-        int phys_next = lookup(0);
-        int issued_k = 0, issued_v = 0;
-        for (int j = 0; j < nt; ++j) {
-            const int stage = j % S;
-            int phys = phys_next;
-            phys_next = lookup(j + 1);
-            const int nbox = boxes_of(j);
-            const int t0 = (j_first + j) * kTok;
-            int row = 0;
-            if (lane < nbox) {
-                const int tok = t0 + (lane / HALVES) * box;  // box | block_size: a box never leaves its block
-                const int lb = tok / p.block_size;
-                if (phys < 0 || phys >= p.num_blocks) {
-                    set_err(p.err, PKV_DEVERR_BLOCK);
-                    phys = 0;
+        const int32_t *tables = p.tables;
+        // Items are numbered sequence by sequence, within a sequence from its
+        // last pair of q tiles (the most keys) to its first, KV head fastest;
+        // CTA c takes items c, c + gridDim.x, ...  The cursor (s_cur, base)
+        // only moves forward: base is the number of the first item of
+        // sequence s_cur.
+        int s_cur = 0;
+        long long base_item = 0;
+        long long idx = blockIdx.x;
+        int it = 0;           // items published
+        int gs = 0;           // K / V steps started (ring position)
+        int issued_k = 0, issued_v = 0, q_issued = 0;  // loads issued
+        bool ok = true;
+        while (ok) {
+            TcItem item;
+            item.nt0 = -1;
+            bool found = false;
+            while (s_cur < p.num_seqs) {
+                const int sl = s_cur + lane;
+                int qb = 0, ql = 0, cnt = 0;
+                if (sl < p.num_seqs) {
+                    qb = p.cu_q[sl];
+                    ql = p.cu_q[sl + 1] - qb;
+                    if (ql > 1) cnt = ((ql + kTiles * R - 1) / (kTiles * R)) * p.hkv;
                 }
-                row = phys * p.block_size + (tok - lb * p.block_size);
+                int inc = cnt;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int t = __shfl_up_sync(0xffffffffu, inc, off);
+                    if (lane >= off) inc += t;
+                }
+                const unsigned hit = __ballot_sync(0xffffffffu, cnt > 0 && idx < base_item + inc);
+                if (hit) {
+                    const int L = __ffs(hit) - 1;
+                    const int cntL = __shfl_sync(0xffffffffu, cnt, L);
+                    base_item += __shfl_sync(0xffffffffu, inc, L) - cntL;
+                    s_cur += L;
+                    item.s = s_cur;
+                    item.q_begin = __shfl_sync(0xffffffffu, qb, L);
+                    item.q_len = __shfl_sync(0xffffffffu, ql, L);
+                    const int r = (int)(idx - base_item);
+                    const int npairs = cntL / p.hkv;
+                    item.kvh = r % p.hkv;
+                    const int pair = npairs - 1 - r / p.hkv;
+                    item.q00 = pair * kTiles * R;
+                    found = true;
+                    break;
+                }
+                base_item += __shfl_sync(0xffffffffu, inc, 31);
+                s_cur += 32;
             }
-            const uint32_t dst_off = (uint32_t)(stage * KVSTAGE + (lane % HALVES) * KVHALF + (lane / HALVES) * box * 128);
-            int okw = 1;
-            if (lane == 0) okw = wait_phase(&k_empty[stage], ((j / S) & 1) ^ 1, &s_abort);
-            if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-            if (lane == 0) mbar_arrive_expect_tx(&k_full[stage], (uint32_t)(nbox * box * 128));
+            if (found) {
+                item.kv_len = p.seq_lens[item.s];
+                if (item.q_len > item.kv_len || (int64_t)item.kv_len > (int64_t)p.max_blocks * p.block_size) {
+                    // flagged once, by the item of the sequence's last pair and KV head 0
+                    if (lane == 0 && item.kvh == 0 && item.q00 + kTiles * R >= item.q_len)
+                        set_err(p.err, PKV_DEVERR_LENGTH);
+                    idx += gridDim.x;
+                    continue;
+                }
+                // the window's first key is lowest for the first row of tile 0,
+                // so both tiles walk from j_first
+                const int lim_first = p.causal ? item.kv_len - item.q_len + item.q00 : item.kv_len - 1;
+                const int lo_first =
+                    (p.window > 0 && lim_first - p.window + 1 > 0) ? lim_first - p.window + 1 : 0;
+                item.j_first = lo_first / kTok;
+                item.nt0 = tile_steps(item, 0);
+                item.nt1 = tile_steps(item, 1);
+            }
+            // publish the item (or the end mark)
+            if (lane == 0) {
+                ok = mbar_wait(&item_empty[it & 1], ((it >> 1) & 1) ^ 1, &s_abort);
+                if (ok) {
+                    s_item[it & 1] = item;
+                    mbar_arrive(&item_full[it & 1]);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+            ++it;
+            if (!ok || !found) break;
+            idx += gridDim.x;
+            const int nt = max(item.nt0, item.nt1);
+            // Q of both tiles, once the previous item's score MMAs have read theirs
+            const int ntiles = item.nt1 > 0 ? 2 : 1;
+            if (lane == 0 && q_issued > 0) ok = mbar_wait(q_empty, (q_issued - 1) & 1, &s_abort);
+            if (!__shfl_sync(0xffffffffu, (int)ok, 0)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(q_full, (uint32_t)(ntiles * G * HALVES * R * 128));
             __syncwarp();
-            if (lane < nbox) tma_load_3d(sk + dst_off, &tmk, &k_full[stage], 0, kvh * HALVES + lane % HALVES, row, pol_kv);
-            issued_k = j + 1;
-            if (lane == 0) okw = wait_phase(&v_empty[stage], ((j / S) & 1) ^ 1, &s_abort);
-            if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-            if (lane == 0) mbar_arrive_expect_tx(&v_full[stage], (uint32_t)(nbox * box * 128));
-            __syncwarp();
-            if (lane < nbox) tma_load_3d(sv + dst_off, &tmv, &v_full[stage], 0, kvh * HALVES + lane % HALVES, row, pol_kv);
-            issued_v = j + 1;
+            for (int t = lane; t < ntiles * G * HALVES; t += 32) {
+                const int u = t / (G * HALVES), g = (t / HALVES) % G, half = t % HALVES;
+                tma_load_3d(sq + u * QTILE + half * QHALF + g * R * 128, &tmq, q_full, 0,
+                            (item.kvh * G + g) * HALVES + half, item.q_begin + item.q00 + u * R, pol_q);
+            }
+            ++q_issued;
+            // K and V tiles: a tile has at most (128 / 16) * HALVES <= 16 boxes:
+            // lane t issues box t of K and of V (sub-block t / HALVES, half t %
+            // HALVES).  Its block-table entry is read one step ahead.
+            const int32_t *trow = tables + (int64_t)item.s * p.max_blocks;
+            auto boxes_of = [&](int j) {
+                const int nvalid = min(kTok, item.kv_len - (item.j_first + j) * kTok);
+                return ((nvalid + box - 1) / box) * HALVES;
+            };
+            auto lookup = [&](int j) -> int {
+                if (j >= nt || lane >= boxes_of(j)) return 0;
+                const int tok = (item.j_first + j) * kTok + (lane / HALVES) * box;
+                return trow[tok / p.block_size];
+            };
+            int phys_next = lookup(0);
+            for (int j = 0; j < nt; ++j, ++gs) {
+                const int stage = gs % S;
+                int phys = phys_next;
+                phys_next = lookup(j + 1);
+                const int nbox = boxes_of(j);
+                const int t0 = (item.j_first + j) * kTok;
+                int row = 0;
+                if (lane < nbox) {
+                    const int tok = t0 + (lane / HALVES) * box;  // box | block_size: a box never leaves its block
+                    const int lb = tok / p.block_size;
+                    if (phys < 0 || phys >= p.num_blocks) {
+                        set_err(p.err, PKV_DEVERR_BLOCK);
+                        phys = 0;
+                    }
+                    row = phys * p.block_size + (tok - lb * p.block_size);
+                }
+                const uint32_t dst_off =
+                    (uint32_t)(stage * KVSTAGE + (lane % HALVES) * KVHALF + (lane / HALVES) * box * 128);
+                int okw = 1;
+                if (lane == 0) okw = wait_phase(&k_empty[stage], ((gs / S) & 1) ^ 1, &s_abort);
+                if (!__shfl_sync(0xffffffffu, okw, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(&k_full[stage], (uint32_t)(nbox * box * 128));
+                __syncwarp();
+                if (lane < nbox)
+                    tma_load_3d(sk + dst_off, &tmk, &k_full[stage], 0, item.kvh * HALVES + lane % HALVES, row, pol_kv);
+                ++issued_k;
+                if (lane == 0) okw = wait_phase(&v_empty[stage], ((gs / S) & 1) ^ 1, &s_abort);
+                if (!__shfl_sync(0xffffffffu, okw, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(&v_full[stage], (uint32_t)(nbox * box * 128));
+                __syncwarp();
+                if (lane < nbox)
+                    tma_load_3d(sv + dst_off, &tmv, &v_full[stage], 0, item.kvh * HALVES + lane % HALVES, row, pol_kv);
+                ++issued_v;
+            }
         }
-        if (issued_v < nt && lane == 0) {
+        if (!ok && lane == 0) {
             // gave up: the loads this warp issued must land before the CTA exits
             s_abort = 1;
             set_err(p.err, PKV_DEVERR_TIMEOUT);
             volatile int never = 0;
-            mbar_wait(q_full, 0, &never);
+            if (q_issued > 0) mbar_wait(q_full, (q_issued - 1) & 1, &never);
             for (int k = issued_k > S ? issued_k - S : 0; k < issued_k; ++k)
                 mbar_wait(&k_full[k % S], (k / S) & 1, &never);
             for (int k = issued_v > S ? issued_v - S : 0; k < issued_v; ++k)
@@ -372,255 +465,308 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ===== MMA issuer: the whole warp walks the loop, one elected lane issues =====
-        {
-            // every lane waits on the same phase; the vote keeps the warp converged
-            auto wait = [&](uint64_t *bar, uint32_t parity) {
-                return __all_sync(0xffffffffu, wait_phase(bar, parity, &s_abort));
-            };
-            const uint32_t idS = idesc_f16(BF ? 1 : 0, 0, 128, kTok);
-            const uint32_t idPV = idesc_f16(BF ? 1 : 0, 1, 128, D);
-            const uint32_t sq_a = smem_u32(sq), sk_a = smem_u32(sk), sv_a = smem_u32(sv);
-            auto issue_s = [&](int u, int j) {
-                const uint32_t kst = sk_a + (j % S) * KVSTAGE;
+        // every lane waits on the same phase; the vote keeps the warp converged
+        auto wait = [&](uint64_t *bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, wait_phase(bar, parity, &s_abort));
+        };
+        const uint32_t idS = idesc_f16(BF ? 1 : 0, 0, 128, kTok);
+        const uint32_t idPV = idesc_f16(BF ? 1 : 0, 1, 128, D);
+        const uint32_t sq_a = smem_u32(sq), sk_a = smem_u32(sk), sv_a = smem_u32(sv);
+        // g: ring position of the K / V step
+        auto issue_s = [&](int u, int g) {
+            const uint32_t kst = sk_a + (g % S) * KVSTAGE;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const int half = kk >> 2, koff = (kk & 3) * 32;
-                    const uint64_t ad = sw128_desc(sq_a + u * QTILE + half * QHALF + koff, 16, 1024);
-                    const uint64_t bd = sw128_desc(kst + half * KVHALF + koff, 16, 1024);
-                    umma_ss(tmem + u * 256, ad, bd, idS, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(s_full(u));
-            };
-            auto issue_pv = [&](int u, int j) {
-                const uint32_t vst = sv_a + (j % S) * KVSTAGE;
-                const uint32_t ts = tmem + u * 256, to = tmem + u * 256 + 128;
-#pragma unroll
-                for (int kk = 0; kk < kTok / 16; ++kk) {
-                    const uint64_t vd = sw128_desc(vst + kk * 2048, KVHALF, 1024);
-                    const uint32_t col = LO ? (kk >> 1) * 32 + (kk & 1) * 8 : kk * 8;
-                    umma_ts(to, ts + col, vd, idPV, (j > 0 || kk > 0) ? 1u : 0u);
-                    if (LO) umma_ts(to, ts + col + 16, vd, idPV, 1u);
-                }
-                umma_commit(o_done(u));
-            };
-            bool ok = wait(q_full, 0) && wait(&k_full[0], 0);
-            if (ok) {
-                tc_fence_after();
-                for (int u = 0; u < kTiles; ++u)
-                    if (steps_of(u) > 0) issue_s(u, 0);
-                umma_commit(&k_empty[0]);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int half = kk >> 2, koff = (kk & 3) * 32;
+                const uint64_t ad = sw128_desc(sq_a + u * QTILE + half * QHALF + koff, 16, 1024);
+                const uint64_t bd = sw128_desc(kst + half * KVHALF + koff, 16, 1024);
+                umma_ss(tmem + u * 256, ad, bd, idS, kk > 0 ? 1u : 0u);
             }
+            umma_commit(s_full(u));
+        };
+        auto issue_pv = [&](int u, int g, bool first) {
+            const uint32_t vst = sv_a + (g % S) * KVSTAGE;
+            const uint32_t ts = tmem + u * 256, to = tmem + u * 256 + 128;
+#pragma unroll
+            for (int kk = 0; kk < kTok / 16; ++kk) {
+                const uint64_t vd = sw128_desc(vst + kk * 2048, KVHALF, 1024);
+                const uint32_t col = LO ? (kk >> 1) * 32 + (kk & 1) * 8 : kk * 8;
+                umma_ts(to, ts + col, vd, idPV, (!first || kk > 0) ? 1u : 0u);
+                if (LO) umma_ts(to, ts + col + 16, vd, idPV, 1u);
+            }
+            umma_commit(o_done(u));
+        };
+        int gc = 0;              // ring position of the current item's first step
+        int tb[kTiles] = {0, 0}; // steps of each tile in earlier items
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+            ok = wait(&item_full[it & 1], (it >> 1) & 1);
+            if (!ok) break;
+            const TcItem item = s_item[it & 1];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_empty[it & 1]);
+            if (item.nt0 < 0) break;
+            const int nt0 = item.nt0, nt1 = item.nt1, nt = max(nt0, nt1);
+            auto steps_of = [&](int u) { return u ? nt1 : nt0; };
+            // V rows past kv_len (only in the last step) are cleared by the first
+            // tile whose P V reads that step
+            const int zt = nt0 == nt ? 0 : 1;
+            ok = wait(q_full, it & 1) && wait(&k_full[gc % S], (gc / S) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            for (int u = 0; u < kTiles && ok; ++u) {
+                if (steps_of(u) == 0) continue;
+                // the scores overwrite the tile's last P of the previous item
+                if (tb[u] > 0) {
+                    ok = wait(o_done(u), (tb[u] - 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                issue_s(u, gc);
+            }
+            if (!ok) break;
+            umma_commit(&k_empty[gc % S]);
+            if (nt == 1) umma_commit(q_empty);  // every score MMA of the item issued
             for (int j = 0; j < nt && ok; ++j) {
-                const uint32_t ph = j & 1;
+                const int g = gc + j;
                 const int j1 = j + 1;
                 bool v_ready = false, k_ready = false;
                 for (int u = 0; u < kTiles && ok; ++u) {
                     if (j >= steps_of(u)) continue;
+                    const uint32_t ph = (uint32_t)(tb[u] + j) & 1;
                     ok = wait(p_full(u), ph);
                     // the last step's V rows past kv_len are cleared by tile zt
-                    if (ok && u != zt && (j_first + j + 1) * kTok > kv_len) ok = wait(p_full(zt), ph);
-                    if (ok && !v_ready) ok = v_ready = wait(&v_full[j % S], (j / S) & 1);
+                    if (ok && u != zt && (item.j_first + j1) * kTok > item.kv_len)
+                        ok = wait(p_full(zt), (uint32_t)(tb[zt] + j) & 1);
+                    if (ok && !v_ready) ok = v_ready = wait(&v_full[g % S], (g / S) & 1);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv(u, j);
+                    issue_pv(u, g, j == 0);
                     if (j1 < steps_of(u)) {
-                        if (!k_ready) ok = k_ready = wait(&k_full[j1 % S], (j1 / S) & 1);
+                        if (!k_ready) ok = k_ready = wait(&k_full[(g + 1) % S], ((g + 1) / S) & 1);
                         // the scores overwrite P of step j: its P V must have completed
                         if (ok) ok = wait(o_done(u), ph);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_s(u, j1);
+                        issue_s(u, g + 1);
                     }
                 }
                 if (!ok) break;
-                umma_commit(&v_empty[j % S]);
-                if (k_ready) umma_commit(&k_empty[j1 % S]);
+                umma_commit(&v_empty[g % S]);
+                if (k_ready) umma_commit(&k_empty[(g + 1) % S]);
+                if (j1 == nt - 1) umma_commit(q_empty);  // every score MMA of the item issued
             }
-            if (!ok && lane == 0) {
-                s_abort = 1;
-                set_err(p.err, PKV_DEVERR_TIMEOUT);
-            }
+            tb[0] += nt0;
+            tb[1] += nt1;
+            gc += nt;
+        }
+        if (!ok && lane == 0) {
+            s_abort = 1;
+            set_err(p.err, PKV_DEVERR_TIMEOUT);
         }
     }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
         // ===== softmax + epilogue: warps 4-7 tile 0, warps 8-11 tile 1, one M row per thread =====
         const int u = (warp - 4) >> 2;
-        const int ntu = steps_of(u);
         const int qw = warp & 3;  // a warp reaches TMEM lanes 32 * (warp % 4) .. + 31
         const int row = qw * 32 + lane;
         const uint32_t trow_addr = tmem + ((uint32_t)(qw * 32) << 16) + u * 256;
         const int g = row / R;
-        const int qi = q00 + u * R + row % R;
-        const bool valid = qi < q_len;
-        const int lim = (p.causal && valid) ? kv_len - q_len + qi : kv_len - 1;
-        const int lo = (p.window > 0 && lim - p.window + 1 > 0) ? lim - p.window + 1 : 0;
         const float sl = p.scale_log2;
-        float m_used = -INFINITY, lsum = 0.f;
+        int tbu = 0;  // steps of this tile in earlier items
+        int gcs = 0;  // ring position of the current item's first step
         bool ok = true;
-        for (int j = 0; j < ntu; ++j) {
-            // warp-uniform outcome: the tcgen05 ld/st below are warp-collective
-            if (!__all_sync(0xffffffffu, wait_phase(s_full(u), j & 1, &s_abort))) {
-                ok = false;
-                break;
-            }
-            // the scores of step j were issued after P V of step j - 1 completed,
-            // so O is settled here and may be rescaled
-            tc_fence_after();
-            const int t0 = (j_first + j) * kTok;
-            // every row of the warp sees every key of the tile: no masking
-            const bool whole = __all_sync(0xffffffffu, t0 + kTok - 1 <= lim && t0 >= lo);
-            // the row's 128 scores, read with one wait (each wait exposes the
-            // whole TMEM load latency)
-            uint32_t sr[kTok];
-#pragma unroll
-            for (int c0 = 0; c0 < kTok; c0 += 32)
-                tmem_ld32(trow_addr + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
-            tmem_wait_ld();
-            if (!whole) {
-#pragma unroll
-                for (int c = 0; c < kTok; ++c) {
-                    const int key = t0 + c;
-                    if (!(key <= lim && key >= lo)) sr[c] = __float_as_uint(-INFINITY);
+        for (int it = 0; ok; ++it) {
+            ok = __all_sync(0xffffffffu, wait_phase(&item_full[it & 1], (it >> 1) & 1, &s_abort));
+            if (!ok) break;
+            const TcItem item = s_item[it & 1];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_empty[it & 1]);
+            if (item.nt0 < 0) break;
+            const int nt = max(item.nt0, item.nt1);
+            const int ntu = u ? item.nt1 : item.nt0;
+            const int zt = item.nt0 == nt ? 0 : 1;
+            const int kv_len = item.kv_len;
+            const int qi = item.q00 + u * R + row % R;
+            const bool valid = qi < item.q_len;
+            const int lim = (p.causal && valid) ? kv_len - item.q_len + qi : kv_len - 1;
+            const int lo = (p.window > 0 && lim - p.window + 1 > 0) ? lim - p.window + 1 : 0;
+            float m_used = -INFINITY, lsum = 0.f;
+            for (int j = 0; j < ntu; ++j) {
+                const int gpos = gcs + j;
+                // warp-uniform outcome: the tcgen05 ld/st below are warp-collective
+                if (!__all_sync(0xffffffffu, wait_phase(s_full(u), (tbu + j) & 1, &s_abort))) {
+                    ok = false;
+                    break;
                 }
-            }
-            // the row max of the raw scores times the scale (positive): eight
-            // independent chains of three-input maxima
-            auto row_max = [&]() -> float {
-                float pm[8];
+                // the scores of step j were issued after P V of step j - 1 completed,
+                // so O is settled here and may be rescaled
+                tc_fence_after();
+                const int t0 = (item.j_first + j) * kTok;
+                // every row of the warp sees every key of the tile: no masking
+                const bool whole = __all_sync(0xffffffffu, t0 + kTok - 1 <= lim && t0 >= lo);
+                // the row's 128 scores, read with one wait (each wait exposes the
+                // whole TMEM load latency)
+                uint32_t sr[kTok];
 #pragma unroll
-                for (int v = 0; v < 8; ++v) pm[v] = fmaxf(__uint_as_float(sr[v]), __uint_as_float(sr[8 + v]));
+                for (int c0 = 0; c0 < kTok; c0 += 32)
+                    tmem_ld32(trow_addr + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
+                tmem_wait_ld();
+                if (!whole) {
 #pragma unroll
-                for (int c = 16; c < kTok; c += 16)
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        pm[v] = fmax3(pm[v], __uint_as_float(sr[c + v]), __uint_as_float(sr[c + 8 + v]));
-                return fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7]))) * sl;
-            };
-            // The running max m_used is taken from the row's first tile with
-            // a visible key and is moved only when p would leave the range
-            // where it is exact enough and finite as a 16-bit value: every p of
-            // a step is at most the step's sum, so a sum <= 2^15 proves all p
-            // <= 2^15.  Otherwise (or on inf / NaN) the row takes the exact
-            // max, O and the row sum are rescaled, and P is written again (a
-            // second pass of the loop below).
-            const bool fresh = m_used == -INFINITY;
-            if (__any_sync(0xffffffffu, fresh) && fresh) m_used = row_max();
-            float step_sum;
-#pragma unroll 1
-            for (int pass = 0;; ++pass) {
-                // p = 2^(s * scale - m_used), written back over the scores as
-                // 16-bit values (the scale and shift, and the row sum, as packed
-                // fp32 pairs).  While a row has met no key yet (a window can
-                // start past whole tiles) every score and m_used are -inf: the
-                // shift is then taken as -inf too, so every p is 0, not NaN.
-                const float neg_m = m_used == -INFINITY ? -INFINITY : -m_used;
-                const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(neg_m, neg_m);
-                float2 ps[4];
-#pragma unroll
-                for (int v = 0; v < 4; ++v) ps[v] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int c0 = 0; c0 < kTok; c0 += 32) {
-                    uint32_t ph[16], pl[16];
-#pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        const float2 x = __ffma2_rn(
-                            make_float2(__uint_as_float(sr[c0 + c]), __uint_as_float(sr[c0 + c + 1])), sl2, nm2);
-                        const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-                        ps[(c >> 1) & 3] = __fadd2_rn(ps[(c >> 1) & 3], make_float2(p0, p1));
-                        const uint32_t h = pack2<T>(p0, p1);
-                        ph[c / 2] = h;
+                    for (int c = 0; c < kTok; ++c) {
+                        const int key = t0 + c;
+                        if (!(key <= lim && key >= lo)) sr[c] = __float_as_uint(-INFINITY);
+                    }
+                }
+                // the row max of the raw scores times the scale (positive): eight
+                // independent chains of three-input maxima
+                auto row_max = [&]() -> float {
+                    float pm[8];
+    #pragma unroll
+                    for (int v = 0; v < 8; ++v) pm[v] = fmaxf(__uint_as_float(sr[v]), __uint_as_float(sr[8 + v]));
+    #pragma unroll
+                    for (int c = 16; c < kTok; c += 16)
+    #pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            pm[v] = fmax3(pm[v], __uint_as_float(sr[c + v]), __uint_as_float(sr[c + 8 + v]));
+                    return fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7]))) * sl;
+                };
+                // The running max m_used is taken from the row's first tile with
+                // a visible key and is moved only when p would leave the range
+                // where it is exact enough and finite as a 16-bit value: every p of
+                // a step is at most the step's sum, so a sum <= 2^15 proves all p
+                // <= 2^15.  Otherwise (or on inf / NaN) the row takes the exact
+                // max, O and the row sum are rescaled, and P is written again (a
+                // second pass of the loop below).
+                const bool fresh = m_used == -INFINITY;
+                if (__any_sync(0xffffffffu, fresh) && fresh) m_used = row_max();
+                float step_sum;
+    #pragma unroll 1
+                for (int pass = 0;; ++pass) {
+                    // p = 2^(s * scale - m_used), written back over the scores as
+                    // 16-bit values (the scale and shift, and the row sum, as packed
+                    // fp32 pairs).  While a row has met no key yet (a window can
+                    // start past whole tiles) every score and m_used are -inf: the
+                    // shift is then taken as -inf too, so every p is 0, not NaN.
+                    const float neg_m = m_used == -INFINITY ? -INFINITY : -m_used;
+                    const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(neg_m, neg_m);
+                    float2 ps[4];
+    #pragma unroll
+                    for (int v = 0; v < 4; ++v) ps[v] = make_float2(0.f, 0.f);
+    #pragma unroll
+                    for (int c0 = 0; c0 < kTok; c0 += 32) {
+                        uint32_t ph[16], pl[16];
+    #pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            const float2 x = __ffma2_rn(
+                                make_float2(__uint_as_float(sr[c0 + c]), __uint_as_float(sr[c0 + c + 1])), sl2, nm2);
+                            const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                            ps[(c >> 1) & 3] = __fadd2_rn(ps[(c >> 1) & 3], make_float2(p0, p1));
+                            const uint32_t h = pack2<T>(p0, p1);
+                            ph[c / 2] = h;
+                            if (LO) {
+                                const float2 hf = unpack2<T>(h);
+                                pl[c / 2] = pack2<T>(p0 - hf.x, p1 - hf.y);
+                            }
+                        }
                         if (LO) {
-                            const float2 hf = unpack2<T>(h);
-                            pl[c / 2] = pack2<T>(p0 - hf.x, p1 - hf.y);
+                            tmem_st16(trow_addr + c0, ph);
+                            tmem_st16(trow_addr + c0 + 16, pl);
+                        } else {
+                            tmem_st16(trow_addr + c0 / 2, ph);
                         }
                     }
-                    if (LO) {
-                        tmem_st16(trow_addr + c0, ph);
-                        tmem_st16(trow_addr + c0 + 16, pl);
-                    } else {
-                        tmem_st16(trow_addr + c0 / 2, ph);
+                    const float2 ps01 = __fadd2_rn(ps[0], ps[1]), ps23 = __fadd2_rn(ps[2], ps[3]);
+                    const float2 ps4 = __fadd2_rn(ps01, ps23);
+                    step_sum = ps4.x + ps4.y;
+                    const bool over = pass == 0 && !(step_sum <= kPSumMax);
+                    if (!__any_sync(0xffffffffu, over)) break;
+                    tmem_wait_st();
+                    float alpha = 1.f;
+                    if (over) {
+                        const float m_new = fmaxf(m_used, row_max());
+                        alpha = fast_exp2(m_used - m_new);
+                        lsum *= alpha;
+                        m_used = m_new;
+                    }
+                    if (j > 0) {
+    #pragma unroll
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t orr[32];
+                            tmem_ld32(trow_addr + 128 + c0, orr);
+                            tmem_wait_ld();
+    #pragma unroll
+                            for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
+                            tmem_st32(trow_addr + 128 + c0, orr);
+                        }
                     }
                 }
-                const float2 ps01 = __fadd2_rn(ps[0], ps[1]), ps23 = __fadd2_rn(ps[2], ps[3]);
-                const float2 ps4 = __fadd2_rn(ps01, ps23);
-                step_sum = ps4.x + ps4.y;
-                const bool over = pass == 0 && !(step_sum <= kPSumMax);
-                if (!__any_sync(0xffffffffu, over)) break;
+                lsum += step_sum;
+                // V rows past kv_len in the last tile hold stale or unrelated data:
+                // zero them, once the tile's TMA load (which may cover some of
+                // them) has landed
+                if (u == zt && t0 + kTok > kv_len) {
+                    if (!wait_phase(&v_full[gpos % S], (gpos / S) & 1, &s_abort)) {
+                        s_abort = 1;
+                        set_err(p.err, PKV_DEVERR_TIMEOUT);
+                    }
+                    if (row >= kv_len - t0) {
+    #pragma unroll
+                        for (int half = 0; half < HALVES; ++half) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(sv + (gpos % S) * KVSTAGE + half * KVHALF + row * 128);
+    #pragma unroll
+                            for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
                 tmem_wait_st();
-                float alpha = 1.f;
-                if (over) {
-                    const float m_new = fmaxf(m_used, row_max());
-                    alpha = fast_exp2(m_used - m_new);
-                    lsum *= alpha;
-                    m_used = m_new;
-                }
-                if (j > 0) {
+                tc_fence_before();
+                mbar_arrive(p_full(u));
+            }
+            if (!ok) break;
+            if (ntu > 0) {
+                ok = __all_sync(0xffffffffu, wait_phase(o_done(u), (tbu + ntu - 1) & 1, &s_abort));
+                if (!ok) break;
+                tc_fence_after();
+                const float inv = 1.f / lsum;
+                const int64_t hq = (int64_t)p.hkv * G;
+                const int64_t off = ((int64_t)(item.q_begin + qi) * hq + (int64_t)item.kvh * G + g) * D;
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t orr[32];
-                        tmem_ld32(trow_addr + 128 + c0, orr);
-                        tmem_wait_ld();
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t orr[32];
+                    tmem_ld32(trow_addr + 128 + c0, orr);
+                    tmem_wait_ld();
+                    if (valid) {
+                        if (p.out_f32) {
+                            float4 *op = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off + c0);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
-                        tmem_st32(trow_addr + 128 + c0, orr);
+                            for (int c = 0; c < 32; c += 4)
+                                op[c / 4] =
+                                    make_float4(__uint_as_float(orr[c]) * inv, __uint_as_float(orr[c + 1]) * inv,
+                                                __uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv);
+                        } else {
+                            uint4 *op = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + off + c0);
+#pragma unroll
+                            for (int c = 0; c < 32; c += 8)
+                                op[c / 8] = make_uint4(
+                                    pack2<T>(__uint_as_float(orr[c]) * inv, __uint_as_float(orr[c + 1]) * inv),
+                                    pack2<T>(__uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv),
+                                    pack2<T>(__uint_as_float(orr[c + 4]) * inv, __uint_as_float(orr[c + 5]) * inv),
+                                    pack2<T>(__uint_as_float(orr[c + 6]) * inv, __uint_as_float(orr[c + 7]) * inv));
+                        }
                     }
                 }
+                // O of this tile has been read: the next item's first P V (which
+                // overwrites O) waits for this warp's next arrival on p_full
+                tc_fence_before();
             }
-            lsum += step_sum;
-            // V rows past kv_len in the last tile hold stale or unrelated data:
-            // zero them, once the tile's TMA load (which may cover some of
-            // them) has landed
-            if (u == zt && t0 + kTok > kv_len) {
-                if (!wait_phase(&v_full[j % S], (j / S) & 1, &s_abort)) {
-                    s_abort = 1;
-                    set_err(p.err, PKV_DEVERR_TIMEOUT);
-                }
-                if (row >= kv_len - t0) {
-#pragma unroll
-                    for (int half = 0; half < HALVES; ++half) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(sv + (j % S) * KVSTAGE + half * KVHALF + row * 128);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(p_full(u));
+            tbu += ntu;
+            gcs += nt;
         }
-        if (ok && ntu > 0) ok = __all_sync(0xffffffffu, wait_phase(o_done(u), (ntu - 1) & 1, &s_abort));
-        if (ok && ntu > 0) {
-            tc_fence_after();
-            const float inv = 1.f / lsum;
-            const int64_t hq = (int64_t)p.hkv * G;
-            const int64_t off = ((int64_t)(q_begin + qi) * hq + (int64_t)kvh * G + g) * D;
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t orr[32];
-                tmem_ld32(trow_addr + 128 + c0, orr);
-                tmem_wait_ld();
-                if (valid) {
-                    if (p.out_f32) {
-                        float4 *op = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off + c0);
-#pragma unroll
-                        for (int c = 0; c < 32; c += 4)
-                            op[c / 4] = make_float4(__uint_as_float(orr[c]) * inv, __uint_as_float(orr[c + 1]) * inv,
-                                                    __uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv);
-                    } else {
-                        uint4 *op = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + off + c0);
-#pragma unroll
-                        for (int c = 0; c < 32; c += 8)
-                            op[c / 8] = make_uint4(
-                                pack2<T>(__uint_as_float(orr[c]) * inv, __uint_as_float(orr[c + 1]) * inv),
-                                pack2<T>(__uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv),
-                                pack2<T>(__uint_as_float(orr[c + 4]) * inv, __uint_as_float(orr[c + 5]) * inv),
-                                pack2<T>(__uint_as_float(orr[c + 6]) * inv, __uint_as_float(orr[c + 7]) * inv));
-                    }
-                }
-            }
-        } else if (ntu > 0 && lane == 0) {
+        if (!ok && lane == 0) {
             s_abort = 1;
             set_err(p.err, PKV_DEVERR_TIMEOUT);
         }
@@ -653,7 +799,12 @@ static pkv_status launch_prefill_tc_t(const CUtensorMap &mq, const CUtensorMap &
     static std::atomic<uint64_t> smem_set{0};
     pkv_status st = set_smem_once(reinterpret_cast<const void *>(kern), smem, &smem_set);
     if (st != PKV_OK) return st;
-    dim3 grid(p.q_tiles, num_seqs, p.hkv);
+    // persistent: one CTA per SM (fewer if there cannot be that many items)
+    int sms = 0;
+    st = sm_count(-1, &sms);
+    if (st != PKV_OK) return st;
+    const int64_t most_items = (int64_t)p.q_tiles * num_seqs * p.hkv;
+    dim3 grid((unsigned)(most_items < sms ? most_items : sms));
     // the register re-balancing inside the kernel needs at least
     // kRegsAtLaunchMin registers per thread at launch, or it would wait forever
     static std::atomic<int> regs{0};
@@ -691,6 +842,7 @@ pkv_status run_prefill_tc(const void *q, int64_t q_stride, const pkv_cache *cach
     p.window = window > 0 ? window : 0;
     const int rows = 128 / p.group;
     p.q_tiles = (max_q_len + kTiles * rows - 1) / (kTiles * rows);
+    p.num_seqs = num_seqs;
     p.box_rows = cache->block_size % 128 == 0  ? 128
                  : cache->block_size % 64 == 0 ? 64
                  : cache->block_size % 32 == 0 ? 32
