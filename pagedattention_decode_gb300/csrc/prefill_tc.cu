@@ -194,6 +194,12 @@ constexpr int kThreads = 384;
 constexpr int kRegsLow = 72;
 constexpr int kRegsHigh = 216;
 constexpr int kRegsAtLaunchMin = (128 * kRegsLow + 256 * kRegsHigh + kThreads - 1) / kThreads;
+// Epilogue staging: each softmax warp passes 16 columns of its 32 O rows
+// through shared memory (row stride 20 floats: conflict-free 16-byte
+// accesses), so the global stores cover 8 rows x 64 contiguous bytes per
+// instruction instead of 32 rows x 16 bytes.
+constexpr int kStageStride = 20;
+constexpr int kStageBytes = 2 * 4 * 32 * kStageStride * 4;
 
 // A work item: the pair of q tiles `pair` (2 x 128 M rows) of KV head `kvh`
 // of the prefill chunk of sequence `s`.  The producer warp finds a CTA's
@@ -230,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sq = base;
     uint8_t *sk = base + kTiles * QTILE;
     uint8_t *sv = sk + S * KVSTAGE;
+    float *stage_o = reinterpret_cast<float *>(sv + S * KVSTAGE + 4096);
     uint64_t *q_full = &bars[0];
     uint64_t *q_empty = &bars[1];  // every score MMA of an item has read its Q
     uint64_t *k_full = &bars[2];
@@ -572,7 +579,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qw = warp & 3;  // a warp reaches TMEM lanes 32 * (warp % 4) .. + 31
         const int row = qw * 32 + lane;
         const uint32_t trow_addr = tmem + ((uint32_t)(qw * 32) << 16) + u * 256;
-        const int g = row / R;
         const float sl = p.scale_log2;
         int tbu = 0;  // steps of this tile in earlier items
         int gcs = 0;  // ring position of the current item's first step
@@ -580,18 +586,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; ok; ++it) {
             ok = __all_sync(0xffffffffu, wait_phase(&item_full[it & 1], (it >> 1) & 1, &s_abort));
             if (!ok) break;
-            const TcItem item = s_item[it & 1];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&item_empty[it & 1]);
-            if (item.nt0 < 0) break;
-            const int nt = max(item.nt0, item.nt1);
-            const int ntu = u ? item.nt1 : item.nt0;
-            const int zt = item.nt0 == nt ? 0 : 1;
-            const int kv_len = item.kv_len;
-            const int qi = item.q00 + u * R + row % R;
-            const bool valid = qi < item.q_len;
-            const int lim = (p.causal && valid) ? kv_len - item.q_len + qi : kv_len - 1;
-            const int lo = (p.window > 0 && lim - p.window + 1 > 0) ? lim - p.window + 1 : 0;
+            // the item is read from shared memory where it is used (few values
+            // stay live across the steps) and released after the epilogue
+            const volatile TcItem &item = s_item[it & 1];
+            const int nt0 = item.nt0, nt1 = item.nt1;
+            if (nt0 < 0) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&item_empty[it & 1]);
+                break;
+            }
+            const int nt = max(nt0, nt1);
+            const int ntu = u ? nt1 : nt0;
+            const int j_first = item.j_first;
+            int lim, lo;
+            bool valid;
+            {
+                const int kv_len = item.kv_len, q_len = item.q_len;
+                const int qi = item.q00 + u * R + row % R;
+                valid = qi < q_len;
+                lim = (p.causal && valid) ? kv_len - q_len + qi : kv_len - 1;
+                lo = (p.window > 0 && lim - p.window + 1 > 0) ? lim - p.window + 1 : 0;
+            }
+            // the step whose V rows past kv_len this tile clears (the item's last
+            // step, when it is partial and this tile is the first to read it), or -1
+            const int zt = nt0 == nt ? 0 : 1;
+            const int jzero = (u == zt && (j_first + nt) * kTok > item.kv_len) ? nt - 1 : -1;
             float m_used = -INFINITY, lsum = 0.f;
             for (int j = 0; j < ntu; ++j) {
                 const int gpos = gcs + j;
@@ -603,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the scores of step j were issued after P V of step j - 1 completed,
                 // so O is settled here and may be rescaled
                 tc_fence_after();
-                const int t0 = (item.j_first + j) * kTok;
+                const int t0 = (j_first + j) * kTok;
                 // every row of the warp sees every key of the tile: no masking
                 const bool whole = __all_sync(0xffffffffu, t0 + kTok - 1 <= lim && t0 >= lo);
                 // the row's 128 scores, read with one wait (each wait exposes the
@@ -707,12 +726,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // V rows past kv_len in the last tile hold stale or unrelated data:
                 // zero them, once the tile's TMA load (which may cover some of
                 // them) has landed
-                if (u == zt && t0 + kTok > kv_len) {
+                if (j == jzero) {
                     if (!wait_phase(&v_full[gpos % S], (gpos / S) & 1, &s_abort)) {
                         s_abort = 1;
                         set_err(p.err, PKV_DEVERR_TIMEOUT);
                     }
-                    if (row >= kv_len - t0) {
+                    if (row >= item.kv_len - t0) {
     #pragma unroll
                         for (int half = 0; half < HALVES; ++half) {
                             uint4 *dst = reinterpret_cast<uint4 *>(sv + (gpos % S) * KVSTAGE + half * KVHALF + row * 128);
@@ -733,36 +752,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const float inv = 1.f / lsum;
                 const int64_t hq = (int64_t)p.hkv * G;
-                const int64_t off = ((int64_t)(item.q_begin + qi) * hq + (int64_t)item.kvh * G + g) * D;
+                float *stg = stage_o + (warp - 4) * 32 * kStageStride;
+                const int rr = lane >> 2, c4 = lane & 3;
+                // the output rows this lane stores: rows k * 8 + rr of the warp
+                int64_t row_off[4];
+                bool row_ok[4];
+                {
+                    const int q_len = item.q_len, q_first = item.q00 + u * R, q_row0 = item.q_begin + q_first;
+                    const int64_t head0 = (int64_t)item.kvh * G;
 #pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int rw = qw * 32 + k * 8 + rr;  // M row of the tile
+                        const int pos = rw % R;
+                        row_ok[k] = q_first + pos < q_len;
+                        row_off[k] = ((int64_t)(q_row0 + pos) * hq + head0 + rw / R) * D + c4 * 4;
+                    }
+                }
+                // a loop, not unrolled: the epilogue runs once per item, and its
+                // code has to come into the instruction cache each time
+#pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t orr[32];
                     tmem_ld32(trow_addr + 128 + c0, orr);
                     tmem_wait_ld();
-                    if (valid) {
-                        if (p.out_f32) {
-                            float4 *op = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off + c0);
 #pragma unroll
-                            for (int c = 0; c < 32; c += 4)
-                                op[c / 4] =
-                                    make_float4(__uint_as_float(orr[c]) * inv, __uint_as_float(orr[c + 1]) * inv,
-                                                __uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv);
-                        } else {
-                            uint4 *op = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + off + c0);
+                    for (int h = 0; h < 2; ++h) {
+                        // this thread's row, 16 columns, into the staging rows
 #pragma unroll
-                            for (int c = 0; c < 32; c += 8)
-                                op[c / 8] = make_uint4(
-                                    pack2<T>(__uint_as_float(orr[c]) * inv, __uint_as_float(orr[c + 1]) * inv),
-                                    pack2<T>(__uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv),
-                                    pack2<T>(__uint_as_float(orr[c + 4]) * inv, __uint_as_float(orr[c + 5]) * inv),
-                                    pack2<T>(__uint_as_float(orr[c + 6]) * inv, __uint_as_float(orr[c + 7]) * inv));
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int c = h * 16 + q4 * 4;
+                            *reinterpret_cast<float4 *>(stg + lane * kStageStride + q4 * 4) =
+                                make_float4(__uint_as_float(orr[c]) * inv, __uint_as_float(orr[c + 1]) * inv,
+                                            __uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv);
                         }
+                        __syncwarp();
+                        // rows k * 8 + rr of the warp, 4 columns per lane: 8 rows x 16 columns per store
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int r = k * 8 + rr;
+                            const float4 v = *reinterpret_cast<const float4 *>(stg + r * kStageStride + c4 * 4);
+                            if (row_ok[k]) {
+                                const int64_t off = row_off[k] + c0 + h * 16;
+                                if (p.out_f32)
+                                    *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off) = v;
+                                else
+                                    *reinterpret_cast<uint2 *>(static_cast<T *>(p.out) + off) =
+                                        make_uint2(pack2<T>(v.x, v.y), pack2<T>(v.z, v.w));
+                            }
+                        }
+                        __syncwarp();
                     }
                 }
                 // O of this tile has been read: the next item's first P V (which
                 // overwrites O) waits for this warp's next arrival on p_full
                 tc_fence_before();
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_empty[it & 1]);
             tbu += ntu;
             gcs += nt;
         }
@@ -793,8 +839,10 @@ static pkv_status launch_prefill_tc_t(const CUtensorMap &mq, const CUtensorMap &
                                       const TcParams &p, int num_seqs, cudaStream_t stream) {
     constexpr int HALVES = D / 64;
     // Q of both tiles + the K and V rings, + 1 KB for the 1024-byte alignment
-    // of the swizzled tiles, + 4 KB of slack after the last stage
-    const int smem = kTiles * HALVES * 128 * 128 + 2 * prefill_stages<D>() * HALVES * kTok * 128 + 1024 + 4096;
+    // of the swizzled tiles, + 4 KB of slack after the last stage, + the
+    // epilogue staging rows
+    const int smem = kTiles * HALVES * 128 * 128 + 2 * prefill_stages<D>() * HALVES * kTok * 128 + 1024 + 4096 +
+                     kStageBytes;
     auto kern = prefill_tc_kernel<D, T>;
     static std::atomic<uint64_t> smem_set{0};
     pkv_status st = set_smem_once(reinterpret_cast<const void *>(kern), smem, &smem_set);
