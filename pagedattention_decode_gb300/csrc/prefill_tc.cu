@@ -633,10 +633,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(trow_addr + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
                 tmem_wait_ld();
                 if (!whole) {
+                    // keys t0 + c with c > lim - t0 (causal limit) or c < lo - t0
+                    // (window start) are invisible; the start only matters on
+                    // steps that begin before it
+                    const int hi_c = lim - t0, lo_c = lo - t0;
 #pragma unroll
-                    for (int c = 0; c < kTok; ++c) {
-                        const int key = t0 + c;
-                        if (!(key <= lim && key >= lo)) sr[c] = __float_as_uint(-INFINITY);
+                    for (int c = 0; c < kTok; ++c)
+                        if (c > hi_c) sr[c] = __float_as_uint(-INFINITY);
+                    if (__any_sync(0xffffffffu, lo_c > 0)) {
+#pragma unroll
+                        for (int c = 0; c < kTok; ++c)
+                            if (c < lo_c) sr[c] = __float_as_uint(-INFINITY);
                     }
                 }
                 // the row max of the raw scores times the scale (positive): eight
