@@ -176,6 +176,16 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volat
     return mbar_test(bar, parity) || mbar_wait(bar, parity, abort);
 }
 
+__device__ __forceinline__ void st_shared_f4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -759,7 +769,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const float inv = 1.f / lsum;
                 const int64_t hq = (int64_t)p.hkv * G;
-                float *stg = stage_o + (warp - 4) * 32 * kStageStride;
+                // shared-window address: the staging accesses are issued as
+                // shared-memory instructions, not generic ones
+                const uint32_t stg = smem_u32(stage_o) + (uint32_t)((warp - 4) * 32 * kStageStride * 4);
                 const int rr = lane >> 2, c4 = lane & 3;
                 // the output rows this lane stores: rows k * 8 + rr of the warp
                 int64_t row_off[4];
@@ -788,16 +800,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             const int c = h * 16 + q4 * 4;
-                            *reinterpret_cast<float4 *>(stg + lane * kStageStride + q4 * 4) =
-                                make_float4(__uint_as_float(orr[c]) * inv, __uint_as_float(orr[c + 1]) * inv,
-                                            __uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv);
+                            st_shared_f4(stg + (uint32_t)((lane * kStageStride + q4 * 4) * 4),
+                                         __uint_as_float(orr[c]) * inv, __uint_as_float(orr[c + 1]) * inv,
+                                         __uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv);
                         }
                         __syncwarp();
                         // rows k * 8 + rr of the warp, 4 columns per lane: 8 rows x 16 columns per store
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const int r = k * 8 + rr;
-                            const float4 v = *reinterpret_cast<const float4 *>(stg + r * kStageStride + c4 * 4);
+                            const float4 v = ld_shared_f4(stg + (uint32_t)((r * kStageStride + c4 * 4) * 4));
                             if (row_ok[k]) {
                                 const int64_t off = row_off[k] + c0 + h * 16;
                                 if (p.out_f32)
