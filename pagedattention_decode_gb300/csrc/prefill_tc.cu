@@ -8,21 +8,27 @@
 // dense contraction, so it runs here as a FlashAttention-style loop on UMMA:
 //
 //  * A q tile = 128 M rows: the G query heads of one KV head x 128/G query
-//    positions (row r -> head r / (128/G), position q0 + r % (128/G)).  A CTA
-//    holds two consecutive tiles, so every K/V tile staged in shared memory
+//    positions (row r -> head r / (128/G), position q0 + r % (128/G)).  A work
+//    item is two consecutive tiles, so every K/V tile staged in shared memory
 //    serves 256 rows.
-//  * Warp 0 streams Q of both tiles once, then 128-token K and V tiles of the
-//    KV head (TMA through the block table, 128-byte swizzle, boxes of the
-//    largest of 128, 64, 32 or 16 rows that divides block_size: L2 -> shared
-//    throughput grows with the box) into separate K and V rings, so a K tile
-//    is released as soon as the scores that read it are done.
-//  * Warp 1, one thread, issues the MMAs: S = Q K^T (M 128, N 128, K 16
-//    steps, both operands K-major from shared memory) into the tile's TMEM
-//    score columns, and O += P V (A = P read from TMEM, B = V as an MN-major
-//    shared operand, N = head_dim) into its TMEM accumulator.  Per step it
-//    issues P V of tile 0, the next scores of tile 0, P V of tile 1, the next
-//    scores of tile 1: while one tile's softmax runs, the tensor pipe works
-//    on the other tile.  Completion is signalled with tcgen05.commit.
+//  * Persistent: one CTA per SM walks its items (c, c + grid, ...; numbered
+//    sequence by sequence, a sequence's pairs of tiles from the last to the
+//    first, KV head fastest).  Warp 0 finds them in cu_seqlens_q, hands each
+//    to the other warps through a two-slot ring in shared memory, and streams
+//    Q of both tiles, then 128-token K and V tiles of the KV head (TMA
+//    through the block table, 128-byte swizzle, boxes of the largest of 128,
+//    64, 32 or 16 rows that divides block_size: L2 -> shared throughput grows
+//    with the box) into separate K and V rings.  Barrier phases run on across
+//    items, so the next item's loads and first scores overlap the current
+//    item's tail.
+//  * Warp 1 issues the MMAs (the whole warp walks the loop, an elected lane
+//    issues): S = Q K^T (M 128, N 128, K 16 steps, both operands K-major
+//    from shared memory) into the tile's TMEM score columns, and O += P V
+//    (A = P read from TMEM, B = V as an MN-major shared operand, N =
+//    head_dim) into its TMEM accumulator.  Per step it issues P V of tile 0,
+//    the next scores of tile 0, P V of tile 1, the next scores of tile 1:
+//    while one tile's softmax runs, the tensor pipe works on the other tile.
+//    Completion is signalled with tcgen05.commit.
 //  * Warps 4-7 (tile 0) and 8-11 (tile 1), one TMEM lane = one M row per
 //    thread, read the 128 scores of their row with a single wait for the
 //    TMEM loads, apply the causal and window limits, keep the
@@ -31,10 +37,10 @@
 //    max comes from the row's first tile with a visible key and is moved only
 //    when a step's p could pass 2^15 (their sum tells, so no per-step max is
 //    taken): then that row of O is rescaled in TMEM and P written again.  The
-//    final O row is divided by the sum and stored.
-// One CTA per SM: all 512 TMEM columns (per tile: S/P 128, O head_dim) and
-// ~197 KB of shared memory; setmaxnreg moves registers from the producer /
-// MMA warpgroup (warps 0-3) to the two softmax warpgroups.
+//    final O row is divided by the sum and stored through shared memory.
+// All 512 TMEM columns (per tile: S/P 128, O head_dim) and ~217 KB of shared
+// memory; setmaxnreg moves registers from the producer / MMA warpgroup
+// (warps 0-3) to the two softmax warpgroups.
 #include <cuda.h>
 
 #include "launch.h"
