@@ -124,6 +124,59 @@ def test_scores_jump_after_the_first_tiles(dtype, factor):
         assert_close(run(case, causal), case.oracle(causal), what=f"jump x{factor} {dtype} causal {causal}")
 
 
+def _spread_lens(n, chunks, seed):
+    """q_len / kv_len of n sequences: prefill chunks at the given indices,
+    decode rows and empty row sets elsewhere."""
+    g = np.random.default_rng(seed)
+    q_lens, kv_lens = [], []
+    for i in range(n):
+        if i in chunks:
+            q = chunks[i]
+            q_lens.append(q)
+            kv_lens.append(q + int(g.integers(0, 300)))
+        elif i % 7 == 3:
+            q_lens.append(0)
+            kv_lens.append(int(g.integers(1, 200)))
+        else:
+            q_lens.append(1)
+            kv_lens.append(int(g.integers(1, 200)))
+    return q_lens, kv_lens
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_chunks_spread_over_many_sequences(causal):
+    """The prefill kernel is persistent: each CTA walks work items (pairs of q
+    tiles x KV heads) found by scanning cu_seqlens_q 32 sequences at a time.
+    Chunks at indices past 32 and 64, between decode rows and empty row sets,
+    with more items (20 pairs x 8 KV heads) than SMs, so some CTAs take two."""
+    chunks = {3: 130, 37: 65, 38: 2, 64: 200, 70: 300, 99: 257}
+    q_lens, kv_lens = _spread_lens(100, chunks, 5)
+    case = varlen_case(150, q_lens, kv_lens, 32, 8, 128, 16)
+    assert_close(run(case, causal), case.oracle(causal), what=f"spread causal {causal}")
+
+
+def test_bad_sequence_is_flagged_and_others_still_right():
+    """A chunk with q_len > kv_len (index 50) is flagged and skipped; every
+    other sequence's rows still match the oracle."""
+    chunks = {2: 70, 50: 40, 80: 129}
+    q_lens, kv_lens = _spread_lens(90, chunks, 6)
+    kv_lens[50] = 20
+    case = varlen_case(151, q_lens, kv_lens, 32, 8, 128, 16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run(case, err=err)
+    assert int(err.item()) & P.DEVERR["length"]
+    # expected rows from the oracle on a copy whose sequence 50 is made valid
+    # (it reads sequence 2's blocks); no other row depends on it
+    import dataclasses
+    tables, lens = case.tables.clone(), case.lens.clone()
+    tables[50] = tables[2]
+    lens[50] = 40
+    want = dataclasses.replace(case, tables=tables, lens=lens).oracle(True)
+    cu = case.cu_q.tolist()
+    rows = [r for s in range(90) if s != 50 for r in range(cu[s], cu[s + 1])]
+    assert_close(got[rows], want[rows], what="rows of the good sequences")
+
+
 @pytest.mark.parametrize("bs", [64, 128, 256])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_large_blocks_use_tall_tma_boxes(bs, dtype):
