@@ -848,12 +848,12 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     if (st != PKV_OK) return st;
     // the merge reads only what the decode kernel wrote: launch it as a
     // programmatic dependent so it is scheduled while the decode kernel drains
-    // few sequences: 4 query heads per merge CTA (more CTAs share a long
-    // sequence's parts); many sequences: 8 (fewer, mostly idle, CTAs)
-    const bool wide = p.num_seqs >= 128;
-    const int mh = wide ? 8 : 4;
-    cudaLaunchConfig_t cfg = {};
+    // many sequences: 8 query heads per merge CTA (fewer, mostly idle, CTAs);
+    // fewer: 4 (more CTAs share a long sequence's parts); so few that even
+    // that leaves SMs idle: 1
     const int hq = p.hkv * p.group;
+    const int mh = p.num_seqs >= 128 ? 8 : (int64_t)p.num_seqs * ((hq + 3) / 4) >= pl.cmax * pl.num_hg ? 4 : 1;
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.num_seqs, (hq + mh - 1) / mh);
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = (size_t)kMergeThreads * sizeof(float4) + (size_t)p.cmax * mh * sizeof(float);
@@ -863,7 +863,7 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    auto merge = wide ? decode_merge_kernel<D, T, 8> : decode_merge_kernel<D, T, 4>;
+    auto merge = mh == 8 ? decode_merge_kernel<D, T, 8> : mh == 4 ? decode_merge_kernel<D, T, 4> : decode_merge_kernel<D, T, 1>;
     PKV_CUDA_TRY(cudaLaunchKernelEx(&cfg, merge, p));
     return PKV_OK;
 }
