@@ -237,12 +237,18 @@ class DecodeStep:
         hg = max(h for h in range(1, min(cap, hkv) + 1) if hkv % h == 0)
         self.num_hg = hkv // hg
 
+    # fused: the new rows are written by the decode kernel (pkv_attn_decode_append)
+    fused = False
+
     def write(self, layer=0):
+        if self.fused:
+            return
         self.P.write_kv(self.k_new, self.v_new, self.slots, self.k_caches[layer], self.v_caches[layer], err=self.err)
 
     def decode(self, layer=0):
+        extra = dict(k_new=self.k_new, v_new=self.v_new) if self.fused else {}
         self.P.attn_decode(self.q, self.k_caches[layer], self.v_caches[layer], self.tables, self.lens, self.w.scale,
-                           out=self.out, workspace=self.ws, err=self.err)
+                           out=self.out, workspace=self.ws, err=self.err, **extra)
 
     def bytes(self):
         """(decode bytes, write bytes) of one layer."""
@@ -754,6 +760,9 @@ def main():
                     help="reference arm: CPU seconds the whole --steps/--warmup run is sized to")
     ap.add_argument("--batch", type=int, default=0,
                     help="use only the first N sequences (a smaller case of the same workload, for profiling)")
+    ap.add_argument("--fused-append", action="store_true",
+                    help="gqa/gpt2/skew: write the new K/V rows inside the decode kernel (pkv_attn_decode_append) "
+                         "instead of pkv_write_kv then pkv_attn_decode")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -789,6 +798,9 @@ def main():
     if args.batch:
         w = W.first_sequences(w, args.batch)
     step = DecodeStepInt8(w, dev) if args.workload == "gqa_int8" else DecodeStep(w, dev)
+    if args.fused_append:
+        assert args.workload != "gqa_int8", "--fused-append: 16-bit caches only"
+        step.fused = True
     use_graph = args.graph == "on" or (args.graph == "auto" and w.layers > 1)
     timer = time_device_graph if use_graph else time_device
     total_ms, dec_ms, wr_ms, clocks = timer(step, args.steps, args.warmup, barrier)
@@ -802,10 +814,12 @@ def main():
 
     peak, peak_kind = measured_peak()
     dec_avg_ms = float(np.mean(dec_ms))
+    if args.fused_append:
+        dec_b += wr_b  # the decode launch also moves the new rows
     achieved = dec_b / (dec_avg_ms * 1e-3) / 1e9
     traffic, digest = profile_traffic()
-    if args.workload != "gqa" or args.batch:
-        traffic = None  # the committed capture covers the full GQA 32/8 workload only
+    if args.workload != "gqa" or args.batch or args.fused_append:
+        traffic = None  # the committed capture covers the full GQA 32/8 workload, write then decode
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -820,7 +834,9 @@ def main():
                    "l2": ("inputs larger than L2 (%.2f GB of K/V per step vs 129 MB), no flush" %
                           (w.layers * sum(w.lengths) * kv_bytes_per_token(
                               w.num_kv_heads, w.head_dim, 1 if args.workload == "gqa_int8" else 2) / 1e9)),
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "write": "in the decode kernel (pkv_attn_decode_append)" if args.fused_append
+                   else "pkv_write_kv then pkv_attn_decode"},
         "tokens_per_s": tokens_per_s,
         "pct_of_hbm": {"nominal_8TBs": 100.0 * value / world / NOMINAL_HBM_GBS,
                        f"{peak_kind}_{peak:.0f}GBs": 100.0 * value / world / peak},
@@ -832,12 +848,13 @@ def main():
                      "algorithmic_bytes_per_launch": dec_b, "avg_launch_ms": dec_avg_ms,
                      "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS, "kernel_source_sha256_16": digest},
         "write_kv": ({"avg_launch_ms": float(np.mean(wr_ms)), "bytes": wr_b,
-                      "GB_per_s": wr_b / (float(np.mean(wr_ms)) * 1e-3) / 1e9} if wr_ms else None),
+                      "GB_per_s": wr_b / (float(np.mean(wr_ms)) * 1e-3) / 1e9}
+                     if wr_ms and not args.fused_append else None),
         "timed_as": "one CUDA graph per step" if use_graph else "eager calls on one stream",
         "clocks": clocks,
-        "gpu_launches": args.steps * 3 * w.layers,
+        "gpu_launches": args.steps * (2 if args.fused_append else 3) * w.layers,
     }
-    if not args.no_e2e and w.layers == 1 and args.workload != "gqa_int8":
+    if not args.no_e2e and w.layers == 1 and args.workload != "gqa_int8" and not args.fused_append:
         n_e2e = max(1, min(args.steps, 200))
         ser_ms, _, _, _ = time_e2e(w, step, n_e2e, 3, barrier, pipelined=False)
         e2e_ms, e2e_bytes, h2d, d2h = time_e2e(w, step, n_e2e, 3, barrier)

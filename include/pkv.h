@@ -249,6 +249,30 @@ PKV_API pkv_status pkv_attn_varlen_window(const void *q, int64_t q_token_stride,
                                           void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
                                           int32_t *err_word, pkv_stream stream);
 
+/* ---- decode with the step's new key / value written in the same call ------- */
+/*
+ * [P2] "Build the block allocator and block tables in PyTorch": a decode step
+ * first stores the new token's key and value in the slot of position
+ * seq_len - 1 of its sequence, then attends over all seq_len keys.  This call
+ * does both in one kernel: row s of k_new / v_new ([num_seqs, num_kv_heads,
+ * head_dim], row s at s * kv_token_stride, 16-byte aligned) is written to
+ * slot table[s][(L - 1) / bs] * bs + (L - 1) % bs of the pools (L =
+ * seq_lens[s]; nothing is written when L == 0), and out is what
+ * pkv_write_kv with those slots followed by pkv_attn_decode_window(window)
+ * gives.  The row is written by the CTA that reads the 16-token sub-block
+ * holding it, before that read; no other CTA reads that sub-block.  A block
+ * id outside [0, num_blocks) in that table entry sets PKV_DEVERR_BLOCK and
+ * the row is not written.  Other arguments, layouts and errors are those of
+ * pkv_attn_decode_window (window <= 0: none); same workspace size.
+ */
+PKV_API pkv_status pkv_attn_decode_append(const void *q, int64_t q_token_stride, const void *k_new,
+                                          const void *v_new, int64_t kv_token_stride, const pkv_cache *cache,
+                                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t *seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                                          float scale, int32_t window, void *out, int32_t out_dtype,
+                                          void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                          pkv_stream stream);
+
 /* ---- int8 KV cache --------------------------------------------------------- */
 /*
  * [P4] section 02, "INT8 KV cache design": keys and values stored as

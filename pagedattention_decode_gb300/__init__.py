@@ -119,10 +119,14 @@ def _workspace(size_fn, workspace: Optional[torch.Tensor], device) -> torch.Tens
 def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                 seq_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
                 out_dtype: torch.dtype = torch.float32, workspace: Optional[torch.Tensor] = None,
-                err: Optional[torch.Tensor] = None, stream=None, window: int = 0) -> torch.Tensor:
+                err: Optional[torch.Tensor] = None, stream=None, window: int = 0,
+                k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None) -> torch.Tensor:
     """q [B, Hq, D]; tables [B, max_blocks] int32; seq_lens [B] int32 -> out [B, Hq, D].
 
-    window > 0 attends only each sequence's most recent ``window`` keys."""
+    window > 0 attends only each sequence's most recent ``window`` keys.
+    With k_new / v_new [B, Hkv, D], row s is first written to the slot of
+    position seq_lens[s] - 1 (from the block table) in the same kernel
+    (pkv_attn_decode_append)."""
     c = _cache(k_cache, v_cache)
     _cuda(q, "q")
     _check_i32(block_tables, "block_tables")
@@ -136,7 +140,20 @@ def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, b
         raise ValueError("out must be contiguous [B, Hq, D]")
     ws = _workspace(lambda: decode_workspace_size(B, hq, c.num_kv_heads, d, q.device.index), workspace, q.device)
     mb = block_tables.shape[1] if block_tables.dim() == 2 else 0
-    if window > 0:
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+            _cuda(t, n)
+            if t.dtype != k_cache.dtype or t.shape != (B, c.num_kv_heads, d):
+                raise ValueError(f"{n} must be [B, Hkv, D] of the cache dtype")
+        if k_new.stride() != v_new.stride() or k_new.stride(1) != d or k_new.stride(2) != 1:
+            raise ValueError("k_new / v_new: rows of contiguous heads, the same stride")
+        check(lib().pkv_attn_decode_append(_ptr(q), _row_stride(q, "q"), _ptr(k_new), _ptr(v_new), k_new.stride(0),
+                                           ctypes.byref(c), _ptr(block_tables), mb, _ptr(seq_lens), B, hq,
+                                           float(scale), int(window), _ptr(out), _DT[out.dtype], _ptr(ws),
+                                           ws.numel() * ws.element_size(), _ptr(err), _stream(stream)))
+    elif window > 0:
         check(lib().pkv_attn_decode_window(_ptr(q), _row_stride(q, "q"), ctypes.byref(c), _ptr(block_tables), mb,
                                            _ptr(seq_lens), B, hq, float(scale), int(window), _ptr(out),
                                            _DT[out.dtype], _ptr(ws), ws.numel() * ws.element_size(), _ptr(err),

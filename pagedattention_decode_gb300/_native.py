@@ -73,6 +73,8 @@ SIGNATURES = {
                                       _i32, _vp, _sz, _vp, _vp]),
     "pkv_attn_varlen_window": (_i32, [_vp, _i64, _P(PkvCache), _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
                                       _f32, _i32, _i32, _vp, _i32, _vp, _sz, _vp, _vp]),
+    "pkv_attn_decode_append": (_i32, [_vp, _i64, _vp, _vp, _i64, _P(PkvCache), _vp, _i32, _vp, _i32, _i32, _f32,
+                                      _i32, _vp, _i32, _vp, _sz, _vp, _vp]),
     "pkv_write_kv_int8": (_i32, [_vp, _vp, _i64, _vp, _i32, _P(PkvCacheI8), _vp, _vp]),
     "pkv_attn_decode_int8": (_i32, [_vp, _i64, _P(PkvCacheI8), _vp, _i32, _vp, _i32, _i32, _f32, _i32, _vp, _i32,
                                     _vp, _sz, _vp, _vp]),

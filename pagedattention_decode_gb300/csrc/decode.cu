@@ -63,6 +63,12 @@ struct DecodeParams {
     int32_t window;                // > 0: attend only the last `window` keys
     const float *k_scale;          // int8 cache: [num_blocks, hkv] scales (NULL for 16-bit caches)
     const float *v_scale;
+    // append mode (16-bit caches): row s of k_new / v_new is the key / value of
+    // position seq_lens[s] - 1 and is written into the pool before the
+    // sub-block holding it is loaded; NULL otherwise
+    const void *k_new, *v_new;
+    int64_t new_stride;            // elements between consecutive new rows
+    void *k_pool, *v_pool;         // the pools ([num_blocks * block_size, hkv, D])
 };
 
 // First key a decode row of a sequence with L keys attends (sliding window).
@@ -277,7 +283,33 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
             }
             const int b1 = (int)(sb + (hi - x) < n_s ? sb + (hi - x) : n_s);
             const int32_t *trow = p.tables + (int64_t)s * p.max_blocks;
-            const int sb0 = decode_first_key(p, p.seq_lens[s]) / kSub;  // window: first sub-block
+            const int L = p.seq_lens[s];
+            const int sb0 = decode_first_key(p, L) / kSub;  // window: first sub-block
+            // append mode: the sub-block holding position L - 1 (the new key);
+            // when this segment reaches it, the new row (this head group's
+            // part) is loaded into registers now, so its latency passes while
+            // the segment's earlier sub-blocks are issued
+            const int sb_new = (!I8 && p.k_new != nullptr) ? (L - 1) / kSub : -1;
+            constexpr int U = D / 8;                 // 16-byte units per head row
+            constexpr int kNewPerLane = 2 * 8 * 16 / 32;  // (K and V) x HG x U / 32, HG * D <= 1024
+            uint4 new_row[kNewPerLane];
+            const bool has_new = sb_new >= sb0 + sb && sb_new < sb0 + b1;
+            if constexpr (!I8) {
+                if (has_new) {
+#pragma unroll
+                    for (int i = 0; i < kNewPerLane; ++i) {
+                        const int t = lane + 32 * i;
+                        if (t < 2 * HG * U) {
+                            const int which = t >= HG * U;
+                            const int tt = which ? t - HG * U : t;
+                            const int head = hg * HG + tt / U;
+                            new_row[i] = *(reinterpret_cast<const uint4 *>(
+                                               static_cast<const T *>(which ? p.v_new : p.k_new) +
+                                               (int64_t)s * p.new_stride + (int64_t)head * D) + tt % U);
+                        }
+                    }
+                }
+            }
             for (int j0 = sb; j0 < b1 && !aborted; j0 += 32) {
                 const int jn = min(32, b1 - j0);
                 int row = 0, pblk = 0;
@@ -302,6 +334,33 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
                     if (!okw) {
                         aborted = true;
                         break;
+                    }
+                    if constexpr (!I8) {
+                        if (sb0 + j0 + j == sb_new) {
+                            // this CTA (and no other of its head group) reads the
+                            // sub-block holding the new key: write its row for
+                            // this group's KV heads first, then let the TMA see it
+                            const int tok = L - 1, lb = tok / p.block_size;
+                            const int phys = trow[lb];
+                            if (phys >= 0 && phys < p.num_blocks) {
+                                const int64_t slot = (int64_t)phys * p.block_size + (tok - lb * p.block_size);
+#pragma unroll
+                                for (int i = 0; i < kNewPerLane; ++i) {
+                                    const int t = lane + 32 * i;
+                                    if (t < 2 * HG * U) {
+                                        const int which = t >= HG * U;
+                                        const int tt = which ? t - HG * U : t;
+                                        const int head = hg * HG + tt / U;
+                                        *(reinterpret_cast<uint4 *>(static_cast<T *>(which ? p.v_pool : p.k_pool) +
+                                                                    (slot * p.hkv + head) * D) + tt % U) = new_row[i];
+                                    }
+                                }
+                                asm volatile("fence.proxy.async.global;" ::: "memory");
+                            } else if (lane == 0) {
+                                set_err(p.err, PKV_DEVERR_BLOCK);
+                            }
+                            __syncwarp();
+                        }
                     }
                     const uint32_t scale_bytes = I8 ? (uint32_t)(8 * p.hkv) : 0u;
                     if (lane == 0) mbar_arrive_expect_tx(&full[stage], stage_bytes + scale_bytes);
@@ -868,11 +927,12 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     return PKV_OK;
 }
 
-// Shared by pkv_attn_decode[_window] (cu_q == NULL) and pkv_attn_varlen[_window] (q_len == 1 rows).
-pkv_status run_decode_window(const void *q, int64_t q_stride, const pkv_cache *cache, const int32_t *tables,
-                             int32_t max_blocks, const int32_t *seq_lens, const int32_t *cu_q, int32_t num_seqs,
-                             int32_t num_q_heads, float scale, int32_t window, void *out, int32_t out_dtype,
-                             void *workspace, size_t workspace_bytes, int32_t *err_word, cudaStream_t stream) {
+// Shared by pkv_attn_decode[_window|_append] (cu_q == NULL) and pkv_attn_varlen[_window] (q_len == 1 rows).
+static pkv_status run_decode_impl(const void *q, int64_t q_stride, const pkv_cache *cache, const int32_t *tables,
+                                  int32_t max_blocks, const int32_t *seq_lens, const int32_t *cu_q, int32_t num_seqs,
+                                  int32_t num_q_heads, float scale, int32_t window, void *out, int32_t out_dtype,
+                                  void *workspace, size_t workspace_bytes, int32_t *err_word, cudaStream_t stream,
+                                  const void *k_new, const void *v_new, int64_t new_stride) {
     DecodePlan pl;
     pkv_status st = make_plan(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, -1, &pl);
     if (st != PKV_OK) return st;
@@ -910,12 +970,25 @@ pkv_status run_decode_window(const void *q, int64_t q_stride, const pkv_cache *c
     p.err = err_word;
     p.stages = pl.stages;
     p.window = window > 0 ? window : 0;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.new_stride = new_stride;
+    p.k_pool = cache->k;
+    p.v_pool = cache->v;
     const bool bf = cache->dtype == PKV_BF16;
     if (cache->head_dim == 64)
         return bf ? launch_decode_t<64, __nv_bfloat16>(mk, mv, p, pl, stream)
                   : launch_decode_t<64, __half>(mk, mv, p, pl, stream);
     return bf ? launch_decode_t<128, __nv_bfloat16>(mk, mv, p, pl, stream)
               : launch_decode_t<128, __half>(mk, mv, p, pl, stream);
+}
+
+pkv_status run_decode_window(const void *q, int64_t q_stride, const pkv_cache *cache, const int32_t *tables,
+                             int32_t max_blocks, const int32_t *seq_lens, const int32_t *cu_q, int32_t num_seqs,
+                             int32_t num_q_heads, float scale, int32_t window, void *out, int32_t out_dtype,
+                             void *workspace, size_t workspace_bytes, int32_t *err_word, cudaStream_t stream) {
+    return run_decode_impl(q, q_stride, cache, tables, max_blocks, seq_lens, cu_q, num_seqs, num_q_heads, scale,
+                           window, out, out_dtype, workspace, workspace_bytes, err_word, stream, nullptr, nullptr, 0);
 }
 
 pkv_status run_decode(const void *q, int64_t q_stride, const pkv_cache *cache, const int32_t *tables,
@@ -1057,6 +1130,26 @@ pkv_status pkv_attn_decode_window(const void *q, int64_t q_token_stride, const p
     if (num_seqs == 0) return ok();
     st = run_decode_window(q, q_token_stride, cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
                            num_q_heads, scale, window, out, out_dtype, workspace, workspace_bytes, err_word, stream);
+    return st == PKV_OK ? ok() : st;
+}
+
+pkv_status pkv_attn_decode_append(const void *q, int64_t q_token_stride, const void *k_new, const void *v_new,
+                                  int64_t kv_token_stride, const pkv_cache *cache, const int32_t *block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs,
+                                  int32_t num_q_heads, float scale, int32_t window, void *out, int32_t out_dtype,
+                                  void *workspace, size_t workspace_bytes, int32_t *err_word, pkv_stream stream) {
+    pkv_status st = check_attention_common(q, q_token_stride, cache, block_tables, max_blocks_per_seq, seq_lens,
+                                           num_seqs, num_q_heads, out, out_dtype, "pkv_attn_decode_append");
+    if (st != PKV_OK) return st;
+    if (num_seqs == 0) return ok();
+    PKV_CHECK_ARG(k_new && v_new, PKV_ERR_INVALID_ARG, "pkv_attn_decode_append: k_new and v_new must be non-NULL");
+    PKV_CHECK_ARG(kv_token_stride >= (int64_t)cache->num_kv_heads * cache->head_dim, PKV_ERR_SHAPE,
+                  "pkv_attn_decode_append: kv_token_stride shorter than a row");
+    PKV_CHECK_ARG(aligned16(k_new) && aligned16(v_new) && kv_token_stride % 8 == 0, PKV_ERR_INVALID_ARG,
+                  "pkv_attn_decode_append: k_new / v_new rows must be 16-byte aligned");
+    st = run_decode_impl(q, q_token_stride, cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
+                         num_q_heads, scale, window, out, out_dtype, workspace, workspace_bytes, err_word, stream, k_new,
+                         v_new, kv_token_stride);
     return st == PKV_OK ? ok() : st;
 }
 

@@ -1,0 +1,96 @@
+"""pkv_attn_decode_append: the step's new key / value written by the decode
+kernel itself, against pkv_write_kv followed by pkv_attn_decode (bit for bit)
+and against the binary64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import pagedattention_decode_gb300 as P
+import workloads as W
+from tests.cases import assert_close, decode_case
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.detach().contiguous().view(torch.int16)
+
+
+def _new_rows(case, seed):
+    B = case.lens.numel()
+    hkv, d = case.k_cache.shape[2], case.k_cache.shape[3]
+    g = W.generator(seed)
+    return (W.normal(g, (B, hkv, d), 1.0, case.dtype), W.normal(g, (B, hkv, d), 1.0, case.dtype))
+
+
+def _slots(case):
+    bs = case.k_cache.shape[1]
+    out = []
+    for s, L in enumerate(case.lens.tolist()):
+        if L == 0:
+            out.append(-1)
+        else:
+            out.append(int(case.tables[s, (L - 1) // bs]) * bs + (L - 1) % bs)
+    return torch.tensor(out, dtype=torch.int64)
+
+
+def _both(case, kn, vn, window=0):
+    """(out, k, v) of the fused call and of write-then-decode, on copies of the pools."""
+    dev = "cuda"
+    q, t, lens = case.q.to(dev), case.tables.to(dev), case.lens.to(dev)
+    k1, v1 = case.k_cache.to(dev), case.v_cache.to(dev)
+    k2, v2 = k1.clone(), v1.clone()
+    out1 = P.attn_decode(q, k1, v1, t, lens, case.scale, window=window, k_new=kn.to(dev), v_new=vn.to(dev))
+    P.write_kv(kn.to(dev), vn.to(dev), _slots(case).to(dev), k2, v2)
+    out2 = P.attn_decode(q, k2, v2, t, lens, case.scale, window=window)
+    torch.cuda.synchronize()
+    return (out1, k1, v1), (out2, k2, v2)
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,dtype", [(32, 8, 128, 16, "f16"), (12, 12, 64, 32, "bf16"),
+                                                (32, 16, 128, 16, "f16"), (8, 2, 64, 64, "bf16")])
+def test_append_equals_write_then_decode(hq, hkv, d, bs, dtype):
+    """Empty and one-key sequences, block-boundary lengths, and a long
+    sequence cut over many CTAs (its new row sits in its last part); with 16
+    KV heads the heads are split over two head groups, each writing its own."""
+    lens = [0, 1, 15, 16, 17, 33, 300, 1000, 40000, 2500]
+    case = decode_case(170 + hkv + bs, lens, hq, hkv, d, bs, dtype)
+    kn, vn = _new_rows(case, 171 + hkv)
+    (o1, k1, v1), (o2, k2, v2) = _both(case, kn, vn)
+    assert torch.equal(_bits(k1), _bits(k2)) and torch.equal(_bits(v1), _bits(v2))
+    assert torch.equal(o1, o2)
+    # and the oracle, on the pools as written
+    from tests.cases import PagedCase
+    written = PagedCase(case.q, k2.cpu(), v2.cpu(), case.tables, case.lens, case.scale, case.dtype)
+    assert_close(o1, written.oracle(), what=f"append {hq}/{hkv}/{d}/{bs}/{dtype}")
+
+
+@pytest.mark.parametrize("window", [1, 17, 4096])
+def test_append_with_window(window):
+    lens = [1, 15, 16, 17, 0, 33, 300, 9000]
+    case = decode_case(180 + window, lens, 32, 8, 128, 16, "f16")
+    kn, vn = _new_rows(case, 181)
+    (o1, k1, v1), (o2, k2, v2) = _both(case, kn, vn, window=window)
+    assert torch.equal(_bits(k1), _bits(k2)) and torch.equal(_bits(v1), _bits(v2))
+    assert torch.equal(o1, o2)
+
+
+def test_append_bad_block_is_flagged_and_not_written():
+    lens = [40, 20]
+    case = decode_case(190, lens, 8, 2, 64, 16, "f16")
+    kn, vn = _new_rows(case, 191)
+    t = case.tables.clone()
+    t[1, (20 - 1) // 16] = case.k_cache.shape[0] + 5  # the new row's block: out of range
+    dev = "cuda"
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    k1, v1 = case.k_cache.to(dev), case.v_cache.to(dev)
+    before = _bits(k1).clone()
+    P.attn_decode(case.q.to(dev), k1, v1, t.to(dev), case.lens.to(dev), case.scale, err=err,
+                  k_new=kn.to(dev), v_new=vn.to(dev))
+    torch.cuda.synchronize()
+    assert int(err.item()) & P.DEVERR["block"]
+    # sequence 0's row was written, nothing else changed
+    slot0 = int(case.tables[0, (40 - 1) // 16]) * 16 + (40 - 1) % 16
+    changed = (_bits(k1) != before).view(-1, 2 * 64).any(dim=1).nonzero().view(-1).tolist()
+    assert changed == [slot0] or changed == []
+    assert torch.equal(k1.view(-1, 2, 64)[slot0].cpu(), kn[0])
