@@ -169,7 +169,9 @@ __device__ __forceinline__ int range_owner(int64_t x, int64_t total, int64_t cta
     return (int)(((x + 1) * ctas - 1) / total);
 }
 
-template <int D, typename T, bool I8>
+// AP: append mode (pkv_attn_decode_append), compiled separately so that the
+// plain decode carries none of its code
+template <int D, typename T, bool I8, bool AP = false>
 __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
     decode_splitk_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                          const DecodeParams p) {
@@ -289,12 +291,12 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
             // when this segment reaches it, the new row (this head group's
             // part) is loaded into registers now, so its latency passes while
             // the segment's earlier sub-blocks are issued
-            const int sb_new = (!I8 && p.k_new != nullptr) ? (L - 1) / kSub : -1;
+            const int sb_new = AP ? (L - 1) / kSub : -1;
             constexpr int U = D / 8;                 // 16-byte units per head row
             constexpr int kNewPerLane = 2 * 8 * 16 / 32;  // (K and V) x HG x U / 32, HG * D <= 1024
             uint4 new_row[kNewPerLane];
             const bool has_new = sb_new >= sb0 + sb && sb_new < sb0 + b1;
-            if constexpr (!I8) {
+            if constexpr (AP) {
                 if (has_new) {
 #pragma unroll
                     for (int i = 0; i < kNewPerLane; ++i) {
@@ -335,7 +337,7 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
                         aborted = true;
                         break;
                     }
-                    if constexpr (!I8) {
+                    if constexpr (AP) {
                         if (sb0 + j0 + j == sb_new) {
                             // this CTA (and no other of its head group) reads the
                             // sub-block holding the new key: write its row for
@@ -895,10 +897,10 @@ static pkv_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, 
     return PKV_OK;
 }
 
-template <int D, typename T, bool I8 = false>
+template <int D, typename T, bool I8 = false, bool AP = false>
 static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
                                   const DecodePlan &pl, cudaStream_t stream) {
-    auto kern = decode_splitk_kernel<D, T, I8>;
+    auto kern = decode_splitk_kernel<D, T, I8, AP>;
     // the plan's shared memory depends only on (D, heads per CTA); size for the largest plan once
     static std::atomic<uint64_t> smem_set{0};
     pkv_status st = set_smem_once(reinterpret_cast<const void *>(kern), 210 * 1024, &smem_set);
@@ -976,6 +978,13 @@ static pkv_status run_decode_impl(const void *q, int64_t q_stride, const pkv_cac
     p.k_pool = cache->k;
     p.v_pool = cache->v;
     const bool bf = cache->dtype == PKV_BF16;
+    if (k_new != nullptr) {
+        if (cache->head_dim == 64)
+            return bf ? launch_decode_t<64, __nv_bfloat16, false, true>(mk, mv, p, pl, stream)
+                      : launch_decode_t<64, __half, false, true>(mk, mv, p, pl, stream);
+        return bf ? launch_decode_t<128, __nv_bfloat16, false, true>(mk, mv, p, pl, stream)
+                  : launch_decode_t<128, __half, false, true>(mk, mv, p, pl, stream);
+    }
     if (cache->head_dim == 64)
         return bf ? launch_decode_t<64, __nv_bfloat16>(mk, mv, p, pl, stream)
                   : launch_decode_t<64, __half>(mk, mv, p, pl, stream);
