@@ -733,8 +733,11 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
 // sequence is cut into ~76 parts), each summing float4 outputs of its parts
 // with four loads in flight, and the part-groups are added in shared memory.
 // Launched as a programmatic dependent of the decode kernel: it is scheduled
-// while that kernel drains and waits for its completion before any read.
-constexpr int kMergeThreads = 512;
+// while that kernel drains and waits for its completion before any read.  Its
+// CTAs are kept small (256 threads, ~40 registers each) so they fit on an SM
+// beside a decode CTA and are waiting there when it finishes; the same code
+// with 512 threads, or with more registers, starts later.
+constexpr int kMergeThreads = 256;
 
 template <int D, typename T, int kMergeHeads>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
