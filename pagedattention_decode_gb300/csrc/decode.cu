@@ -32,6 +32,8 @@
 #include "launch.h"
 #include "ptx.cuh"
 
+#include <type_traits>
+
 namespace pkv {
 
 constexpr int kSub = 16;      // tokens per stage (the mma M dimension)
@@ -414,6 +416,13 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
     const int G = p.group;
     const int g = lane >> 2, t4 = lane & 3;
     const int hA = 2 * t4, hB = 2 * t4 + 1;
+    // int8 cache with G = 2 or 4: MMA columns G .. 2G - 1 repeat heads
+    // 0 .. G - 1 and carry the low 16-bit part of their P, so P V takes one
+    // MMA per m tile instead of two; the two parts of O are added at the end
+    // of the segment (lanes t4 and t4 + G / 2 hold a head's two parts)
+    const bool packlo = I8 && (G == 2 || G == 4);
+    const int gcols = packlo ? 2 * G : G;  // MMA columns that hold a head
+    const bool lo_lane = packlo && t4 >= (G >> 1);
     const float sl = p.scale_log2;
     const int qheads_cta = HG * G;
     int it = 0;
@@ -436,10 +445,11 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
         // query fragments: B operand (16 dims x 8 heads), head g of the group
         uint32_t qf[D / 16][2];
         {
-            const T *qp = static_cast<const T *>(p.q) + qrow * p.q_stride + (int64_t)(kvh * G + g) * D;
+            const int qcol = g < G ? g : (g < gcols ? g - G : 0);  // the head in column g
+            const T *qp = static_cast<const T *>(p.q) + qrow * p.q_stride + (int64_t)(kvh * G + qcol) * D;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                if (g < G) {
+                if (g < gcols) {
                     // int8: dims permuted inside each 16-dim step to match the K codes' byte order
                     qf[kk][0] = *reinterpret_cast<const uint32_t *>(qp + kk * 16 + (I8 ? 4 * t4 : 2 * t4));
                     qf[kk][1] = *reinterpret_cast<const uint32_t *>(qp + kk * 16 + (I8 ? 4 * t4 + 2 : 8 + 2 * t4));
@@ -546,13 +556,17 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
                 if (g < nlo) x0 = x1 = -INFINITY;
                 if (g + 8 < nlo) x2 = x3 = -INFINITY;
             }
-            if (hA >= G) x0 = x2 = 0.f;
-            if (hB >= G) x1 = x3 = 0.f;
+            if (hA >= gcols) x0 = x2 = 0.f;
+            if (hB >= gcols) x1 = x3 = 0.f;
             float bA = fmaxf(x0, x2), bB = fmaxf(x1, x3);
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 bA = fmaxf(bA, __shfl_xor_sync(0xffffffffu, bA, off));
                 bB = fmaxf(bB, __shfl_xor_sync(0xffffffffu, bB, off));
+            }
+            if (packlo) {  // both columns of a head keep one running max
+                bA = fmaxf(bA, __shfl_xor_sync(0xffffffffu, bA, G >> 1));
+                bB = fmaxf(bB, __shfl_xor_sync(0xffffffffu, bB, G >> 1));
             }
             const float nA = fmaxf(mA, bA), nB = fmaxf(mB, bB);
             const float aA = fast_exp2(mA - nA), aB = fast_exp2(mB - nB);
@@ -562,12 +576,16 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
             const float p2 = fast_exp2(x2 - nA), p3 = fast_exp2(x3 - nB);
             lA = lA * aA + p0 + p2;
             lB = lB * aB + p1 + p3;
+            // int8 (closer to issue-bound): skipped when no max of the warp moved,
+            // which leaves O exactly as multiplying by 1 would
+            if (!I8 || __any_sync(0xffffffffu, aA != 1.f || aB != 1.f)) {
 #pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-                o[mt][0] *= aA;
-                o[mt][1] *= aB;
-                o[mt][2] *= aA;
-                o[mt][3] *= aB;
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    o[mt][0] *= aA;
+                    o[mt][1] *= aB;
+                    o[mt][2] *= aA;
+                    o[mt][3] *= aB;
+                }
             }
             // P as the B operand (16 tokens x 8 heads), hi and lo 16-bit parts
             // (int8: P is scaled by the block's V scale, so the codes multiply directly)
@@ -579,8 +597,7 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
             const uint32_t h01 = pack2<T>(q0, q1), h23 = pack2<T>(q2, q3);
             const float2 r01 = unpack2<T>(h01), r23 = unpack2<T>(h23);
             const uint32_t l01 = pack2<T>(q0 - r01.x, q1 - r01.y), l23 = pack2<T>(q2 - r23.x, q3 - r23.y);
-            const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-            const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+            const uint32_t bh0 = movmatrix_trans(lo_lane ? l01 : h01), bh1 = movmatrix_trans(lo_lane ? l23 : h23);
             uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
             if (nv < kSub) {
                 m01 = (2 * t4 < nv ? 0x0000ffffu : 0u) | (2 * t4 + 1 < nv ? 0xffff0000u : 0u);
@@ -590,32 +607,39 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
             if constexpr (I8) {
                 // codes of 16 tokens x 32 dims per ldmatrix.x4.trans; M row g of an
                 // m tile is dim 2g, row g + 8 is dim 2g + 1 (see the output mapping)
-                const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
+                auto pv_i8 = [&](auto lo_pass, uint32_t bl0, uint32_t bl1) {
+                    const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-                for (int m2 = 0; m2 < D / 32; ++m2) {
-                    const int chunk = 2 * m2 + (lane >> 4);
-                    uint32_t r[4];
-                    ldmatrix_x4_trans(r, smem_u32(vb + tok * 128 + ((chunk ^ (tok & 7)) << 4)));
+                    for (int m2 = 0; m2 < D / 32; ++m2) {
+                        const int chunk = 2 * m2 + (lane >> 4);
+                        uint32_t r[4];
+                        ldmatrix_x4_trans(r, smem_u32(vb + tok * 128 + ((chunk ^ (tok & 7)) << 4)));
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const uint32_t lo = r[2 * u] ^ 0x80808080u, hi = r[2 * u + 1] ^ 0x80808080u;
-                        uint32_t a[4];
-                        if constexpr (BIAS) {
-                            a[0] = i8_pair_biased(lo, 0x4240u);
-                            a[1] = i8_pair_biased(lo, 0x4341u);
-                            a[2] = i8_pair_biased(hi, 0x4240u);
-                            a[3] = i8_pair_biased(hi, 0x4341u);
-                        } else {
-                            a[0] = i8_pair<T>(lo, 0x4240u);
-                            a[1] = i8_pair<T>(lo, 0x4341u);
-                            a[2] = i8_pair<T>(hi, 0x4240u);
-                            a[3] = i8_pair<T>(hi, 0x4341u);
+                        for (int u = 0; u < 2; ++u) {
+                            const uint32_t lo = r[2 * u] ^ 0x80808080u, hi = r[2 * u + 1] ^ 0x80808080u;
+                            uint32_t a[4];
+                            if constexpr (BIAS) {
+                                a[0] = i8_pair_biased(lo, 0x4240u);
+                                a[1] = i8_pair_biased(lo, 0x4341u);
+                                a[2] = i8_pair_biased(hi, 0x4240u);
+                                a[3] = i8_pair_biased(hi, 0x4341u);
+                            } else {
+                                a[0] = i8_pair<T>(lo, 0x4240u);
+                                a[1] = i8_pair<T>(lo, 0x4341u);
+                                a[2] = i8_pair<T>(hi, 0x4240u);
+                                a[3] = i8_pair<T>(hi, 0x4341u);
+                            }
+                            mma_16816<T>(o[2 * m2 + u], a, bh0, bh1);
+                            if constexpr (decltype(lo_pass)::value) mma_16816<T>(o[2 * m2 + u], a, bl0, bl1);
                         }
-                        mma_16816<T>(o[2 * m2 + u], a, bh0, bh1);
-                        mma_16816<T>(o[2 * m2 + u], a, bl0, bl1);
                     }
-                }
+                };
+                if (packlo)
+                    pv_i8(std::false_type{}, 0u, 0u);
+                else
+                    pv_i8(std::true_type{}, movmatrix_trans(l01), movmatrix_trans(l23));
             } else {
+                const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
                 const int tok = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
@@ -639,6 +663,12 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
                 set_err(p.err, PKV_DEVERR_TIMEOUT);
             }
             return;
+        }
+        if (packlo) {  // O of a head = its high-part column + its low-part column
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[mt][e] += __shfl_xor_sync(0xffffffffu, o[mt][e], G >> 1);
         }
         // sum over the 8 lanes holding other tokens of the same heads
 #pragma unroll
