@@ -171,6 +171,10 @@ __device__ __forceinline__ int range_owner(int64_t x, int64_t total, int64_t cta
     return (int)(((x + 1) * ctas - 1) / total);
 }
 
+// int8 decode: how far (log2 units) a score may pass the running max before
+// the max is moved
+constexpr float kLazyMax = 8.f;
+
 // AP: append mode (pkv_attn_decode_append), compiled separately so that the
 // plain decode carries none of its code
 template <int D, typename T, bool I8, bool AP = false>
@@ -558,27 +562,36 @@ __global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
             }
             if (hA >= gcols) x0 = x2 = 0.f;
             if (hB >= gcols) x1 = x3 = 0.f;
-            float bA = fmaxf(x0, x2), bB = fmaxf(x1, x3);
+            // int8 (closer to issue-bound): the running max is lazy.  It moves
+            // only when a score of the warp passes it by more than kLazyMax (so
+            // every p <= 2^kLazyMax); a vote stands in for the reduction on the
+            // other tiles.  O, l (and the records) stay relative to the max used.
+            bool moved = true;
+            if constexpr (I8)
+                moved = __any_sync(0xffffffffu, !(fmaxf(x0, x2) <= mA + kLazyMax) || !(fmaxf(x1, x3) <= mB + kLazyMax));
+            float aA = 1.f, aB = 1.f;
+            if (moved) {
+                float bA = fmaxf(x0, x2), bB = fmaxf(x1, x3);
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                bA = fmaxf(bA, __shfl_xor_sync(0xffffffffu, bA, off));
-                bB = fmaxf(bB, __shfl_xor_sync(0xffffffffu, bB, off));
+                for (int off = 4; off < 32; off <<= 1) {
+                    bA = fmaxf(bA, __shfl_xor_sync(0xffffffffu, bA, off));
+                    bB = fmaxf(bB, __shfl_xor_sync(0xffffffffu, bB, off));
+                }
+                if (packlo) {  // both columns of a head keep one running max
+                    bA = fmaxf(bA, __shfl_xor_sync(0xffffffffu, bA, G >> 1));
+                    bB = fmaxf(bB, __shfl_xor_sync(0xffffffffu, bB, G >> 1));
+                }
+                const float nA = fmaxf(mA, bA), nB = fmaxf(mB, bB);
+                aA = fast_exp2(mA - nA);
+                aB = fast_exp2(mB - nB);
+                mA = nA;
+                mB = nB;
             }
-            if (packlo) {  // both columns of a head keep one running max
-                bA = fmaxf(bA, __shfl_xor_sync(0xffffffffu, bA, G >> 1));
-                bB = fmaxf(bB, __shfl_xor_sync(0xffffffffu, bB, G >> 1));
-            }
-            const float nA = fmaxf(mA, bA), nB = fmaxf(mB, bB);
-            const float aA = fast_exp2(mA - nA), aB = fast_exp2(mB - nB);
-            mA = nA;
-            mB = nB;
-            const float p0 = fast_exp2(x0 - nA), p1 = fast_exp2(x1 - nB);
-            const float p2 = fast_exp2(x2 - nA), p3 = fast_exp2(x3 - nB);
+            const float p0 = fast_exp2(x0 - mA), p1 = fast_exp2(x1 - mB);
+            const float p2 = fast_exp2(x2 - mA), p3 = fast_exp2(x3 - mB);
             lA = lA * aA + p0 + p2;
             lB = lB * aB + p1 + p3;
-            // int8 (closer to issue-bound): skipped when no max of the warp moved,
-            // which leaves O exactly as multiplying by 1 would
-            if (!I8 || __any_sync(0xffffffffu, aA != 1.f || aB != 1.f)) {
+            if (moved) {
 #pragma unroll
                 for (int mt = 0; mt < D / 16; ++mt) {
                     o[mt][0] *= aA;

@@ -81,6 +81,28 @@ def test_int8_decode_matches_oracle(hq, hkv, bs, dtype, window):
     assert_close(out, want, what=f"int8 {hq}/{hkv}/{bs}/{dtype}/w{window}")
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_int8_decode_rising_and_jumping_scores(dtype):
+    """Key scales that grow block by block, so the scores keep rising along
+    each sequence and the running max moves on many tiles (split sequences
+    included), and one late block whose scores jump far above all others."""
+    lens = [5000, 700, 33, 16, 2100]
+    q, kq, vq, ks, vs, tables, L = _int8_case(720, lens, 32, 8, 16, dtype)
+    ks = ks.copy()
+    for i, n in enumerate(lens):
+        nblk = W.blocks_for(n, 16)
+        for j in range(nblk):
+            ks[tables[i, j], :] = 0.002 * (1 + j)
+        if nblk > 20:
+            ks[tables[i, nblk - 10], :] = 1.0
+    dk, dv, dks, dvs = _dev(kq, vq, ks, vs)
+    out = P.attn_decode_int8(q.cuda(), dk, dv, dks, dvs, torch.from_numpy(tables).cuda(), torch.from_numpy(L).cuda(),
+                             128 ** -0.5)
+    torch.cuda.synchronize()
+    want = oracle.paged_attention_int8(q, dtype, kq, vq, ks, vs, tables, L, 128 ** -0.5)
+    assert_close(out, want, what=f"int8 rising {dtype}")
+
+
 def test_int8_decode_long_split_and_16bit_out():
     lens = [30000, 5, 4000]
     q, kq, vq, ks, vs, tables, L = _int8_case(700, lens, 32, 8, 16, "f16")
