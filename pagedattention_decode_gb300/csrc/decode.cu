@@ -42,6 +42,16 @@ constexpr int kTile = 2048;   // bytes of one swizzled 16-token x 64-element til
 // accumulators in registers (3 warps per SM sub-partition), 16 at head_dim 64.
 template <int D>
 constexpr int max_heads_per_cta() { return D == 64 ? 16 : 8; }
+
+// int8 cache: three CTAs of four KV heads (five warps) per SM.  The SM's
+// warps then spread evenly over its four sub-partitions, four each, which
+// leaves each thread 128 registers (with two CTAs of eight heads, five warps
+// share a sub-partition and 96 registers are the most a thread can have).
+constexpr int kI8CtasPerSm = 3;
+constexpr int kI8HeadsPerCta = 4;
+
+template <int D, bool I8>
+constexpr int cta_threads() { return 32 * (1 + (I8 ? kI8HeadsPerCta : max_heads_per_cta<D>())); }
 constexpr int kMinSubBlocksPerCta = 4;
 
 struct DecodeParams {
@@ -178,7 +188,7 @@ constexpr float kLazyMax = 8.f;
 // AP: append mode (pkv_attn_decode_append), compiled separately so that the
 // plain decode carries none of its code
 template <int D, typename T, bool I8, bool AP = false>
-__global__ void __launch_bounds__(32 * (1 + max_heads_per_cta<D>()), I8 ? 2 : 1)
+__global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : 1)
     decode_splitk_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                          const DecodeParams p) {
     // 2 KB shared tiles per KV head per sub-block: 16 tokens x 64 dims of a
@@ -909,7 +919,7 @@ struct DecodePlan {
 
 static int pick_heads_per_cta(int hkv, int head_dim, bool i8) {
     const int halves = i8 ? 1 : head_dim / 64;  // 2 KB tiles per head per K (or V)
-    const int cap = head_dim == 64 ? max_heads_per_cta<64>() : max_heads_per_cta<128>();
+    const int cap = i8 ? kI8HeadsPerCta : head_dim == 64 ? max_heads_per_cta<64>() : max_heads_per_cta<128>();
     for (int hg = cap < hkv ? cap : hkv; hg >= 1; --hg)
         if (hkv % hg == 0 && hg * halves * 2 * kTile <= 64 * 1024) return hg;
     return 1;
@@ -925,9 +935,9 @@ static pkv_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, 
     pl->heads_per_cta = pick_heads_per_cta(hkv, head_dim, i8);
     pl->num_hg = hkv / pl->heads_per_cta;
     // persistent: all CTAs resident at once -- one per SM over all head
-    // groups, two per SM for int8 (half-size stages: more consumer warps per
-    // SM to hide the code conversion)
-    const int per_sm = i8 ? 2 : 1;
+    // groups, three per SM for int8 (smaller stages: more consumer warps per
+    // SM to hide the code conversion, and registers enough for each)
+    const int per_sm = i8 ? kI8CtasPerSm : 1;
     pl->cmax = per_sm * sms / pl->num_hg > 0 ? per_sm * sms / pl->num_hg : 1;
     const int stage_bytes = pl->heads_per_cta * (i8 ? 1 : head_dim / 64) * 2 * kTile;
     int ns = (200 * 1024 / per_sm) / stage_bytes;
