@@ -288,7 +288,9 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : 1)
     if (warp == 0) {
         // ===== producer =====
         const uint64_t pol = policy_evict_first();
-        int it = 0;
+        int it = 0;  // loads issued; ring position (stage, phase) kept alongside without a division
+        int pstage = 0;
+        uint32_t pphase = 0;
         bool aborted = false;
         int s = s_first_seq;
         int sb = (int)(lo - s_first_start);
@@ -345,9 +347,9 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : 1)
                 for (int j = 0; j < jn; ++j) {
                     const int r = __shfl_sync(0xffffffffu, row, j);
                     const int rb = __shfl_sync(0xffffffffu, pblk, j);
-                    const int stage = it % NS;
+                    const int stage = pstage;
                     int okw = 1;
-                    if (lane == 0) okw = mbar_wait(&empty[stage], ((it / NS) & 1) ^ 1, &s_abort);
+                    if (lane == 0) okw = mbar_wait(&empty[stage], pphase ^ 1u, &s_abort);
                     okw = __shfl_sync(0xffffffffu, okw, 0);
                     if (!okw) {
                         aborted = true;
@@ -400,6 +402,10 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : 1)
                                     pol);
                     }
                     ++it;
+                    if (++pstage == NS) {
+                        pstage = 0;
+                        pphase ^= 1u;
+                    }
                 }
             }
             x += b1 - sb;
@@ -439,7 +445,8 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : 1)
     const bool lo_lane = packlo && t4 >= (G >> 1);
     const float sl = p.scale_log2;
     const int qheads_cta = HG * G;
-    int it = 0;
+    int stage = 0;  // ring position of the next sub-block and the parity of its fill
+    uint32_t phase = 0;
     bool first_seg = true;
     int s = s_first_seq;
     int sb = (int)(lo - s_first_start);
@@ -495,9 +502,8 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : 1)
         for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
         bool aborted = false;
-        for (int j = sb; j < b1; ++j, ++it) {
-            const int stage = it % NS;
-            if (!mbar_wait(&full[stage], (it / NS) & 1, &s_abort)) {
+        for (int j = sb; j < b1; ++j) {
+            if (!mbar_wait(&full[stage], phase, &s_abort)) {
                 aborted = true;
                 break;
             }
@@ -679,6 +685,10 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == NS) {
+                stage = 0;
+                phase ^= 1u;
+            }
         }
         if (aborted) {
             if (lane == 0) {
