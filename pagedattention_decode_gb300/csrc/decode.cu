@@ -43,12 +43,14 @@ constexpr int kTile = 2048;   // bytes of one swizzled 16-token x 64-element til
 template <int D>
 constexpr int max_heads_per_cta() { return D == 64 ? 16 : 8; }
 
-// int8 cache: three CTAs of four KV heads (five warps) per SM.  The SM's
-// warps then spread evenly over its four sub-partitions, four each, which
-// leaves each thread 128 registers (with two CTAs of eight heads, five warps
-// share a sub-partition and 96 registers are the most a thread can have).
-constexpr int kI8CtasPerSm = 3;
-constexpr int kI8HeadsPerCta = 4;
+// int8 cache: two CTAs of up to eight KV heads (nine warps) per SM.  With
+// eight KV heads a stage then holds whole 16-token rows of the pool, and
+// sixteen consumer warps hide the code conversion.  Measured against the other
+// shapes the registers allow (same code; GB/s of codes at GQA 32/8, B 256):
+// 2 x 8 heads 6,075 (96 registers, a few bytes spilled), 2 x 4 6,016 and
+// 3 x 4 5,990 (128+ registers, no spills), 4 x 4 5,877, 1 x 8 4,820.
+constexpr int kI8CtasPerSm = 2;
+constexpr int kI8HeadsPerCta = 8;
 
 template <int D, bool I8>
 constexpr int cta_threads() { return 32 * (1 + (I8 ? kI8HeadsPerCta : max_heads_per_cta<D>())); }
@@ -945,8 +947,8 @@ static pkv_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, 
     pl->heads_per_cta = pick_heads_per_cta(hkv, head_dim, i8);
     pl->num_hg = hkv / pl->heads_per_cta;
     // persistent: all CTAs resident at once -- one per SM over all head
-    // groups, three per SM for int8 (smaller stages: more consumer warps per
-    // SM to hide the code conversion, and registers enough for each)
+    // groups, two per SM for int8 (half-size stages: more consumer warps per
+    // SM to hide the code conversion)
     const int per_sm = i8 ? kI8CtasPerSm : 1;
     pl->cmax = per_sm * sms / pl->num_hg > 0 ? per_sm * sms / pl->num_hg : 1;
     const int stage_bytes = pl->heads_per_cta * (i8 ? 1 : head_dim / 64) * 2 * kTile;
