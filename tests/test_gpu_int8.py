@@ -67,7 +67,8 @@ def _int8_case(seed, lens, hq, hkv, bs, dtype, nb=None):
 
 
 @pytest.mark.parametrize("hq,hkv,bs,dtype", [(32, 8, 16, "f16"), (32, 8, 32, "bf16"), (32, 4, 16, "f16"),
-                                             (8, 8, 16, "bf16"), (16, 8, 16, "f16"), (8, 4, 32, "bf16")])
+                                             (8, 8, 16, "bf16"), (16, 8, 16, "f16"), (8, 4, 32, "bf16"),
+                                             (32, 16, 16, "f16"), (48, 12, 16, "bf16")])
 @pytest.mark.parametrize("window", [0, 100])
 def test_int8_decode_matches_oracle(hq, hkv, bs, dtype, window):
     lens = [1, 15, 16, 17, 33, 300, 1000, 2500] + [0]
