@@ -41,7 +41,15 @@ constexpr int kTile = 2048;   // bytes of one swizzled 16-token x 64-element til
 // Consumer warps (one per KV head) per CTA: 8 at head_dim 128 keeps the
 // accumulators in registers (3 warps per SM sub-partition), 16 at head_dim 64.
 template <int D>
-constexpr int max_heads_per_cta() { return D == 64 ? 16 : 8; }
+constexpr int max_heads_per_cta() { return D == 64 ? 4 : 8; }
+// 16-bit caches with head_dim 64: three CTAs of up to four KV heads (five
+// warps) per SM.  Small D 64 calls are latency-bound, and more, smaller CTAs
+// start streaming sooner.  Measured on the GPT-2-shaped step (12 layers, 12
+// heads, B 32, contexts 64-1024; ms per step, without / with the new rows
+// written by the decode kernel): 1 x 12 heads 0.2214 / 0.2136, 2 x 6
+// 0.2196 / 0.2050, 3 x 4 0.2158 / 0.2050, 4 x 3 0.2173 / 0.2071, 6 x 2
+// 0.2235 / 0.2127.
+constexpr int kD64CtasPerSm = 3;
 
 // int8 cache: two CTAs of up to eight KV heads (nine warps) per SM.  With
 // eight KV heads a stage then holds whole 16-token rows of the pool, and
@@ -190,7 +198,7 @@ constexpr float kLazyMax = 8.f;
 // AP: append mode (pkv_attn_decode_append), compiled separately so that the
 // plain decode carries none of its code
 template <int D, typename T, bool I8, bool AP = false>
-__global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : 1)
+__global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : (D == 64 ? kD64CtasPerSm : 1))
     decode_splitk_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                          const DecodeParams p) {
     // 2 KB shared tiles per KV head per sub-block: 16 tokens x 64 dims of a
@@ -947,9 +955,9 @@ static pkv_status make_plan(int32_t num_seqs, int32_t num_q_heads, int32_t hkv, 
     pl->heads_per_cta = pick_heads_per_cta(hkv, head_dim, i8);
     pl->num_hg = hkv / pl->heads_per_cta;
     // persistent: all CTAs resident at once -- one per SM over all head
-    // groups, two per SM for int8 (half-size stages: more consumer warps per
-    // SM to hide the code conversion)
-    const int per_sm = i8 ? kI8CtasPerSm : 1;
+    // groups (head_dim 128), two per SM for int8 (half-size stages: more
+    // consumer warps per SM to hide the code conversion), three for head_dim 64
+    const int per_sm = i8 ? kI8CtasPerSm : (head_dim == 64 ? kD64CtasPerSm : 1);
     pl->cmax = per_sm * sms / pl->num_hg > 0 ? per_sm * sms / pl->num_hg : 1;
     const int stage_bytes = pl->heads_per_cta * (i8 ? 1 : head_dim / 64) * 2 * kTile;
     int ns = (200 * 1024 / per_sm) / stage_bytes;
