@@ -191,8 +191,8 @@ __device__ __forceinline__ int range_owner(int64_t x, int64_t total, int64_t cta
     return (int)(((x + 1) * ctas - 1) / total);
 }
 
-// int8 decode: how far (log2 units) a score may pass the running max before
-// the max is moved
+// Lazy running max (int8 and head_dim 128): how far (log2 units) a score may
+// pass the running max before the max is moved
 constexpr float kLazyMax = 8.f;
 
 // AP: append mode (pkv_attn_decode_append), compiled separately so that the
@@ -446,11 +446,15 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : (D =
     const int G = p.group;
     const int g = lane >> 2, t4 = lane & 3;
     const int hA = 2 * t4, hB = 2 * t4 + 1;
-    // int8 cache with G = 2 or 4: MMA columns G .. 2G - 1 repeat heads
-    // 0 .. G - 1 and carry the low 16-bit part of their P, so P V takes one
+    // head_dim 128 and int8: MMA columns G .. 2G - 1 repeat heads 0 .. G - 1
+    // (G = 2 or 4) and carry the low 16-bit part of their P, so P V takes one
     // MMA per m tile instead of two; the two parts of O are added at the end
-    // of the segment (lanes t4 and t4 + G / 2 hold a head's two parts)
-    const bool packlo = I8 && (G == 2 || G == 4);
+    // of the segment (lanes t4 and t4 + G / 2 hold a head's two parts).  The
+    // running max of these kernels is lazy (below).  The head_dim 64 kernel,
+    // latency-bound on small calls, keeps the plain form: with these paths
+    // compiled in, its GPT-2-shaped step measured 1-2% slower.
+    constexpr bool kLazy = I8 || D == 128;
+    const bool packlo = kLazy && (G == 2 || G == 4);
     const int gcols = packlo ? 2 * G : G;  // MMA columns that hold a head
     const bool lo_lane = packlo && t4 >= (G >> 1);
     const float sl = p.scale_log2;
@@ -588,12 +592,12 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : (D =
             }
             if (hA >= gcols) x0 = x2 = 0.f;
             if (hB >= gcols) x1 = x3 = 0.f;
-            // int8 (closer to issue-bound): the running max is lazy.  It moves
-            // only when a score of the warp passes it by more than kLazyMax (so
-            // every p <= 2^kLazyMax); a vote stands in for the reduction on the
-            // other tiles.  O, l (and the records) stay relative to the max used.
+            // kLazy: the running max is lazy.  It moves only when a score of the
+            // warp passes it by more than kLazyMax (so every p <= 2^kLazyMax); a
+            // vote stands in for the reduction and the rescale on the other
+            // tiles.  O, l (and the records) stay relative to the max used.
             bool moved = true;
-            if constexpr (I8)
+            if constexpr (kLazy)
                 moved = __any_sync(0xffffffffu, !(fmaxf(x0, x2) <= mA + kLazyMax) || !(fmaxf(x1, x3) <= mB + kLazyMax));
             float aA = 1.f, aB = 1.f;
             if (moved) {
@@ -677,7 +681,7 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : (D =
                     pv_i8(std::false_type{}, 0u, 0u);
                 else
                     pv_i8(std::true_type{}, movmatrix_trans(l01), movmatrix_trans(l23));
-            } else {
+            } else if constexpr (!kLazy) {
                 const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
                 const int tok = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
@@ -692,6 +696,26 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : (D =
                     mma_16816<T>(o[mt], a, bh0, bh1);
                     mma_16816<T>(o[mt], a, bl0, bl1);
                 }
+            } else {
+                auto pv16 = [&](auto lo_pass, uint32_t bl0, uint32_t bl1) {
+                    const int tok = (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        const int cg = mt * 2 + ((lane >> 3) & 1);
+                        uint32_t a[4];
+                        ldmatrix_x4_trans(a, smem_u32(vb + (cg >> 3) * kTile + tok * 128 + (((cg & 7) ^ (tok & 7)) << 4)));
+                        a[0] &= m01;
+                        a[1] &= m01;
+                        a[2] &= m23;
+                        a[3] &= m23;
+                        mma_16816<T>(o[mt], a, bh0, bh1);
+                        if constexpr (decltype(lo_pass)::value) mma_16816<T>(o[mt], a, bl0, bl1);
+                    }
+                };
+                if (packlo)
+                    pv16(std::false_type{}, 0u, 0u);
+                else
+                    pv16(std::true_type{}, movmatrix_trans(l01), movmatrix_trans(l23));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
