@@ -23,7 +23,7 @@ What it follows:
   every id and retains each; a shared block is copied on the first divergent
   write.
 
-Readings where the pages are silent or at odds (each listed in the design doc):
+Readings where the pages are silent or at odds:
 
 * refcounts and the free stack meet as follows: releasing the last reference
   pushes the id back on the stack (page 1 parks zero-ref blocks until an LRU
