@@ -10,10 +10,12 @@
 //
 //  * Work split (split-K, "flash-decoding"): the 16-token sub-blocks of all
 //    sequences are concatenated and cut into equal contiguous ranges, one per
-//    CTA, one CTA per SM (persistent).  A sequence wholly inside one range is
-//    finished in place; a sequence cut by a range boundary leaves (running max,
-//    running sum, unnormalised output) records in the workspace that
-//    decode_merge_kernel combines.  Balance is exact whatever the length mix.
+//    CTA, all CTAs resident at once (persistent: one per SM for head_dim 128,
+//    two for int8 caches, three for head_dim 64).  A sequence wholly inside
+//    one range is finished in place; a sequence cut by a range boundary
+//    leaves (running max, running sum, unnormalised output) records in the
+//    workspace that decode_merge_kernel combines.  Balance is exact whatever
+//    the length mix.
 //  * Data movement: one producer warp walks the block tables and issues TMA
 //    tensor loads (one 16-token x 64-dim tile, 2 KB, 128-byte swizzle, per KV
 //    head and half of head_dim) into a ring of shared-memory stages guarded by
@@ -26,7 +28,10 @@
 //    sum and accumulator) follows the online-normaliser recurrence of Milakov &
 //    Gimelshein (2018) as used by FlashAttention-2; P is transposed in
 //    registers (movmatrix) and multiplied with V^T on the tensor cores as a
-//    16-bit hi + lo pair, so P keeps ~16 significant bits.
+//    16-bit hi + lo pair, so P keeps ~16 significant bits (with 2 or 4 query
+//    heads per KV head both parts share one MMA: the N = 8 columns hold each
+//    head twice).  For head_dim 128 and int8 the running max is lazy: it moves
+//    only when a scaled score passes it by more than 8 in base 2 (p <= 256).
 #include <cuda.h>
 
 #include "launch.h"
