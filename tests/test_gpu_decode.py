@@ -37,6 +37,8 @@ SHAPES = [
     (8, 8, 128, 64, "bf16"),
     (24, 24, 64, 16, "f16"),   # two KV-head groups per sequence
     (2, 1, 128, 128, "f16"),
+    (16, 8, 128, 16, "bf16"),  # 2 per KV head, both parts of P in one MMA
+    (64, 16, 128, 16, "f16"),  # 4 per KV head, two head groups of 8 KV heads
 ]
 
 
