@@ -101,3 +101,46 @@ def assert_close(got: torch.Tensor, want: np.ndarray, tol: float = TOL, what: st
     worst = float(err.max()) if err.size else 0.0
     assert (err <= bound).all(), f"{what}: max abs err {worst:.3e} at {np.unravel_index(err.argmax(), err.shape)}"
     return worst
+
+
+def _u16(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+class Subset:
+    """Host copy of the blocks a set of sequences use, with ids renumbered; the
+    oracle replays writes and copies on it and attends over it."""
+
+    def __init__(self, k_cache, v_cache, table_rows):
+        ids = sorted({int(b) for row in table_rows for b in row if b >= 0})
+        self.local = {b: i for i, b in enumerate(ids)}
+        idx = torch.tensor(ids, dtype=torch.long, device=k_cache.device)
+        self.k = _u16(k_cache[idx]).copy()
+        self.v = _u16(v_cache[idx]).copy()
+        self.bs = k_cache.shape[1]
+
+    def table(self, row):
+        return [self.local[int(b)] for b in row if b >= 0]
+
+    def write(self, slots, k, v):
+        keep = [(i, s) for i, s in enumerate(slots) if s // self.bs in self.local]
+        if not keep:
+            return
+        loc = [self.local[s // self.bs] * self.bs + s % self.bs for _, s in keep]
+        rows = torch.tensor([i for i, _ in keep])
+        oracle.write_kv(k[rows], v[rows], loc, self.k, self.v)
+
+    def copy(self, pairs):
+        loc = [(self.local[s], self.local[d]) for s, d in pairs if s in self.local and d in self.local]
+        if loc:
+            oracle.copy_blocks(self.k, self.v, loc)
+
+    def attend(self, q_rows, table_rows, lens, scale, dtype, cu_q=None):
+        """Binary64 attention over the host copy: one row per sequence, or
+        packed causal rows when cu_q is given."""
+        mb = max(len(t) for t in table_rows)
+        tab = np.full((len(table_rows), mb), -1, dtype=np.int32)
+        for i, t in enumerate(table_rows):
+            tab[i, :len(t)] = t
+        return oracle.paged_attention(q_rows, self.k, self.v, dtype, tab, np.array(lens, dtype=np.int32), scale,
+                                      cu_q=cu_q, causal=cu_q is not None)

@@ -1,10 +1,12 @@
 """pkv_attn_decode_append: the step's new key / value written by the decode
 kernel itself, against pkv_write_kv followed by pkv_attn_decode (bit for bit)
-and against the binary64 oracle."""
+and against the binary64 oracle (pools written by the oracle's slot write on
+host copies, then binary64 attention)."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import pagedattention_decode_gb300 as P
 import workloads as W
 from tests.cases import assert_close, decode_case
@@ -14,6 +16,16 @@ pytestmark = pytest.mark.gpu
 
 def _bits(t):
     return t.detach().contiguous().view(torch.int16)
+
+
+def _u16(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _oracle_pools(case, kn, vn):
+    ok, ov = _u16(case.k_cache).copy(), _u16(case.v_cache).copy()
+    oracle.write_kv(kn, vn, _slots(case).tolist(), ok, ov)
+    return ok, ov
 
 
 def _new_rows(case, seed):
@@ -59,10 +71,12 @@ def test_append_equals_write_then_decode(hq, hkv, d, bs, dtype):
     (o1, k1, v1), (o2, k2, v2) = _both(case, kn, vn)
     assert torch.equal(_bits(k1), _bits(k2)) and torch.equal(_bits(v1), _bits(v2))
     assert torch.equal(o1, o2)
-    # and the oracle, on the pools as written
-    from tests.cases import PagedCase
-    written = PagedCase(case.q, k2.cpu(), v2.cpu(), case.tables, case.lens, case.scale, case.dtype)
-    assert_close(o1, written.oracle(), what=f"append {hq}/{hkv}/{d}/{bs}/{dtype}")
+    # and the oracle: the new rows written into host copies of the pools by
+    # the oracle's own slot write, then binary64 attention over them
+    ok, ov = _oracle_pools(case, kn, vn)
+    assert np.array_equal(_u16(k1), ok) and np.array_equal(_u16(v1), ov)
+    want = oracle.paged_attention(case.q, ok, ov, case.dtype, case.tables.numpy(), case.lens.numpy(), case.scale)
+    assert_close(o1, want, what=f"append {hq}/{hkv}/{d}/{bs}/{dtype}")
 
 
 @pytest.mark.parametrize("window", [1, 17, 4096])
@@ -73,6 +87,11 @@ def test_append_with_window(window):
     (o1, k1, v1), (o2, k2, v2) = _both(case, kn, vn, window=window)
     assert torch.equal(_bits(k1), _bits(k2)) and torch.equal(_bits(v1), _bits(v2))
     assert torch.equal(o1, o2)
+    ok, ov = _oracle_pools(case, kn, vn)
+    assert np.array_equal(_u16(k1), ok) and np.array_equal(_u16(v1), ov)
+    want = oracle.paged_attention(case.q, ok, ov, case.dtype, case.tables.numpy(), case.lens.numpy(), case.scale,
+                                  window=window)
+    assert_close(o1, want, what=f"append, window {window}")
 
 
 def test_append_bad_block_is_flagged_and_not_written():

@@ -7,7 +7,7 @@ import torch
 
 import pagedattention_decode_gb300 as P
 import workloads as W
-from tests.cases import TOL, assert_close, decode_case
+from tests.cases import TOL, Subset, assert_close, decode_case
 
 pytestmark = pytest.mark.gpu
 
@@ -148,9 +148,11 @@ def test_gqa_mapping_contiguous_groups():
 
 
 @pytest.mark.parametrize("wl", [W.gqa_decode, W.long_skewed_decode])
-def test_full_size_workload_sampled(wl):
-    """The full-size workloads, launched as the bench launches them; sampled
-    sequences checked against the oracle one by one."""
+def test_full_size_workload_every_sequence(wl):
+    """The full-size workloads, launched as the bench launches them; every
+    sequence checked against the oracle, those the even split of sub-blocks
+    cuts over several CTAs (their outputs come from the merge) included."""
+    import bench
     w = wl()
     dev = "cuda"
     kc = W.normal_device(w.seed * 10 + 1, (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim), w.sigma,
@@ -160,22 +162,15 @@ def test_full_size_workload_sampled(wl):
     q = W.normal(g, (w.batch, w.num_q_heads, w.head_dim), w.sigma, w.dtype)
     tables, _ = W.scattered_tables(g, w.lengths, w.block_size, w.num_blocks)
     lens = torch.tensor(w.lengths, dtype=torch.int32)
-    rng = np.random.default_rng(w.seed)
-    picks = sorted(set(rng.choice(w.batch, size=min(6, w.batch), replace=False).tolist()) | {w.batch - 1})
-    # copy the sampled sequences' blocks to the host before any kernel of ours runs
-    samples = []
-    for i in picks:
-        nbk = W.blocks_for(w.lengths[i], w.block_size)
-        ids = tables[i, :nbk].long()
-        samples.append((i, kc[ids.to(dev)].cpu(), vc[ids.to(dev)].cpu()))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert bench.split_records(w.lengths, sms) > 0   # some sequences are cut
+    rows = [tables[i].tolist() for i in range(w.batch)]
+    sub = Subset(kc, vc, rows)   # before any kernel of ours runs
     out = P.attn_decode(q.to(dev), kc, vc, tables.to(dev), lens.to(dev), w.scale)
     torch.cuda.synchronize()
-    from tests.cases import PagedCase
-    for i, ksub, vsub in samples:
-        nbk = ksub.shape[0]
-        case = PagedCase(q[i:i + 1], ksub, vsub, torch.arange(nbk, dtype=torch.int32).view(1, -1),
-                         lens[i:i + 1], w.scale, w.dtype)
-        assert_close(out[i:i + 1], case.oracle(), what=f"{w.name} seq {i}")
+    del kc, vc
+    want = sub.attend(q, [sub.table(r) for r in rows], w.lengths, w.scale, w.dtype)
+    assert_close(out, want, what=w.name)
 
 
 @pytest.mark.parametrize("window", [1, 15, 16, 17, 100, 4096])

@@ -5,8 +5,10 @@ embeds libpkv in a process whose device memory belongs to another runtime's
 allocator, or a loop that must not call cudaMalloc because that synchronises
 the device.  The no-allocation entry point keeps its scratch in a fixed array
 inside the library instead.  These tests call it through the C ABI and
-compare it with the workspace entry point, twice in a row (the array keeps
-the previous call's contents), and check that an over-size call is refused.
+compare it with the workspace entry point (bit for bit: the same plan and
+kernels) and with the binary64 oracle, twice in a row (the array keeps the
+previous call's contents), and check that a call one sequence past the
+array's size is refused.
 
 This file is collected last so that a failure here, under -x, comes after
 every other test has run.
@@ -18,7 +20,7 @@ import torch
 
 import pagedattention_decode_gb300 as P
 from pagedattention_decode_gb300 import _native
-from tests.cases import TOL, decode_case
+from tests.cases import assert_close, decode_case
 
 pytestmark = pytest.mark.gpu
 
@@ -61,23 +63,38 @@ def _no_alloc(c):
 def test_no_alloc_matches_workspace_entry_point_twice():
     # two different calls in a row: many sequences cut by the split (records
     # in the scratch), then another shape and dtype over the same array
-    first = decode_case(901, [1, 700, 64, 3000, 17, 0, 2048, 5] * 12, 32, 8, 128, 16, "f16").to("cuda")
-    second = decode_case(902, [40000, 9, 333], 24, 12, 64, 32, "bf16", sigma=0.5).to("cuda")
+    first = decode_case(901, [1, 700, 64, 3000, 17, 0, 2048, 5] * 12, 32, 8, 128, 16, "f16")
+    second = decode_case(902, [40000, 9, 333], 24, 12, 64, 32, "bf16", sigma=0.5)
     for c in (first, second):
-        want = _with_workspace(c)
-        got = _no_alloc(c)
+        dc = c.to("cuda")
+        want = _with_workspace(dc)
+        got = _no_alloc(dc)
         torch.cuda.synchronize()
-        assert (got - want).abs().max().item() <= TOL
+        assert torch.equal(got, want)
+        assert_close(got, c.oracle(), what="no-allocation decode")
 
 
 def test_no_alloc_refuses_oversize_call():
-    c = decode_case(903, [20, 30], 8, 2, 64, 16, "f16").to("cuda")
+    """The scratch holds the split-K records (they grow with the device's SM
+    count, the query heads and head_dim) and 4 bytes per sequence.  At head_dim
+    64 the size query's answer is the 16-bit plan the call checks: the
+    smallest batch whose need passes the array's size is refused on the host,
+    before anything is launched."""
+    hq, hkv, d = 32, 4, 64
+    limit = _native.PKV_NOALLOC_SCRATCH_BYTES
+    need = lambda b: P.decode_workspace_size(b, hq, hkv, d)
+    lo, hi = 1, 1 << 26          # need(lo) <= limit < need(hi)
+    assert need(lo) <= limit < need(hi)
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        lo, hi = (mid, hi) if need(mid) <= limit else (lo, mid)
+    c = decode_case(903, [20, 30], hq, hkv, d, 16, "f16").to("cuda")
     L = _native.lib()
     cache = _cache(c)
-    out = torch.empty((2, 8, 64), dtype=torch.float32, device="cuda")
-    # ten million sequences need more scratch than the fixed array holds: the
-    # call is refused on the host before anything is launched
-    st = L.pkv_attn_decode_noalloc(c.q.data_ptr(), 8 * 64, ctypes.byref(cache), c.tables.data_ptr(),
-                                   c.tables.shape[1], c.lens.data_ptr(), 10_000_000, 8, c.scale, out.data_ptr(),
+    out = torch.empty((2, hq, d), dtype=torch.float32, device="cuda")
+    st = L.pkv_attn_decode_noalloc(c.q.data_ptr(), hq * d, ctypes.byref(cache), c.tables.data_ptr(),
+                                   c.tables.shape[1], c.lens.data_ptr(), hi, hq, c.scale, out.data_ptr(),
                                    _native.PKV_F32, None, None)
-    assert st == 8 and b"fixed array" in L.pkv_last_error()
+    msg = L.pkv_last_error()   # read before the next library call replaces it
+    assert st == 8 and b"fixed array" in msg
+    assert str(need(hi)).encode() in msg
