@@ -182,7 +182,10 @@ PKV_API pkv_status pkv_attn_decode(const void *q, int64_t q_token_stride, const 
  * sequences or query heads) returns PKV_ERR_WORKSPACE and launches nothing.
  * The first call on a device looks up the array's address on the current
  * device (cudaGetSymbolAddress); make that first call before any stream
- * capture.  All calls share the one array and nothing needs clearing between
+ * capture.  A reset of the device (cudaDeviceReset, or another teardown of
+ * its primary context) loads the library's module again, possibly at another
+ * address: the first call after it looks the address up again, so it too
+ * belongs before any capture.  All calls share the one array and nothing needs clearing between
  * them, but calls that overlap on the GPU (other streams, other threads) race
  * on it.  The call itself allocates nothing.
  */

@@ -19,6 +19,7 @@ STATUS = {
     7: "PKV_ERR_CUDA", 8: "PKV_ERR_WORKSPACE", 9: "PKV_ERR_UNSUPPORTED",
 }
 PKV_F16, PKV_BF16, PKV_F32 = 0, 1, 2
+PKV_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # the fixed scratch of pkv_attn_decode_noalloc (pkv.h)
 DEVERR = {"slot": 0x1, "block": 0x2, "pair": 0x4, "timeout": 0x8, "length": 0x10}
 
 

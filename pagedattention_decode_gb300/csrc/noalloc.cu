@@ -13,6 +13,8 @@
 // All calls share it: the kernels write every byte they later read, so nothing
 // is cleared between calls, and two calls that run on the GPU at the same time
 // (on different streams, or from different host threads) race on it.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "launch.h"
@@ -36,23 +38,63 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[PKV_NOALLOC_SCRATCH_B
 namespace {
 constexpr int kMaxDevices = 256;
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
+// Per device: the address found for the context that was current then, and
+// that context's process-unique id.  cudaDeviceReset (or any teardown of the
+// primary context) loads the module again, possibly at another address, in a
+// context with a new id, so the next call looks the address up again.
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void *ptr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Id of the current context, or 0 (and a lookup on every call) when the
+// driver does not offer it.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
 }  // namespace
 
 // Device address of the scratch array on `device`, which must be current.
-// The first call per device looks it up (cudaGetSymbolAddress) and caches it.
+// Set-up: the first call on a device (and the first after the device's
+// context was re-created) looks it up with cudaGetSymbolAddress and keeps it.
 static pkv_status scratch_address(int device, void **out) {
     PKV_CHECK_ARG(device >= 0 && device < kMaxDevices, PKV_ERR_UNSUPPORTED, "device ordinal %d", device);
+    // cudaGetDevice already made the device's primary context current
+    const unsigned long long id = current_context_id();
     std::lock_guard<std::mutex> g(g_scratch_mu);
-    if (g_scratch_ptr[device] == nullptr) {
+    ScratchEntry &e = g_scratch[device];
+    if (e.ptr == nullptr || id == 0 || e.ctx_id != id) {
         void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        PKV_CHECK_ARG(e == cudaSuccess && p != nullptr, PKV_ERR_CUDA,
+        cudaError_t r = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        PKV_CHECK_ARG(r == cudaSuccess && p != nullptr, PKV_ERR_CUDA,
                       "cudaGetSymbolAddress of the no-allocation scratch on device %d: %s", device,
-                      cudaGetErrorString(e));
-        g_scratch_ptr[device] = p;
+                      cudaGetErrorString(r));
+        e.ptr = p;
+        e.ctx_id = id;
     }
-    *out = g_scratch_ptr[device];
+    *out = e.ptr;
     return PKV_OK;
 }
 
