@@ -17,6 +17,15 @@ device time of the step with all inputs resident in HBM.  The KV bytes
 copied from pinned host memory and the output copied back inside the timed
 region, and the host allocator producing slots and tables every step.
 
+The same JSON line carries ``configs``: every other workload of the scope
+table, each in a short block of its own (median of 100 iterations, 50 for the
+mixed step), with its roofline, the clocks sampled inside its timed window
+and its CPU oracle baseline (all cores and one core): the tiny MHA decode,
+the GPT-2-shaped 12-layer step, the long/skewed contexts, the GQA step over an
+int8 cache, and the mixed packed step (prefill chunks + decode rows, then a
+width-4 beam split with copy-on-write).  Clocks come from NVML (read only)
+sampled every few ms and while the GPU drains the enqueued work.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun each rank runs an independent replica (the path has no
 exchange step); rank 0 prints one JSON line.
@@ -25,6 +34,7 @@ exchange step); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -99,32 +109,107 @@ def write_bytes(tokens, hkv, d, dtype_bytes):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
+    """SM clock, its maximum, board power and the clock-event reasons, read
+    (never set) through NVML -- ctypes on libnvidia-ml, every few ms on a
+    thread -- with nvidia-smi's polling as the fallback.  Every sample carries
+    the host time it was taken; ``summary(t0, t1)`` keeps the samples of one
+    timed window, and ``poll_until(event)`` samples from the calling thread
+    while the GPU drains the work already enqueued (so a window of a few ms
+    still gets samples under load)."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clocks-event reason bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu: str):
+    def __init__(self, gpu: str, period_s: float = 0.004):
         self.gpu = gpu
-        self.lines = []
+        self.period = period_s
+        self.samples = []  # (host time, sm MHz, max sm MHz, power W, [reasons])
         self.proc = None
+        self.nvml = None
+        self.stop = threading.Event()
+        self.thread = None
+
+    # -- NVML ---------------------------------------------------------------
+    def _open_nvml(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByUUID(self.gpu.encode(), ctypes.byref(h)) != 0:
+                if not self.gpu.isdigit() or lib.nvmlDeviceGetHandleByIndex_v2(int(self.gpu), ctypes.byref(h)) != 0:
+                    return None
+            try:
+                reasons = lib.nvmlDeviceGetCurrentClocksEventReasons
+            except AttributeError:
+                reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError):
+            return None
+        c = ctypes
+        sm, mx, pw, rs = c.c_uint(), c.c_uint(), c.c_uint(), c.c_ulonglong()
+
+        def read():
+            if lib.nvmlDeviceGetClockInfo(h, 1, c.byref(sm)) != 0:  # NVML_CLOCK_SM
+                return None
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, c.byref(mx))
+            p = pw.value / 1000.0 if lib.nvmlDeviceGetPowerUsage(h, c.byref(pw)) == 0 else None
+            act = [nm for bit, nm in self.REASONS.items() if rs.value & bit] if reasons(h, c.byref(rs)) == 0 else []
+            return (time.perf_counter(), float(sm.value), float(mx.value), p, act)
+
+        return read if read() is not None else None
+
+    def sample(self):
+        if self.nvml is not None:
+            s = self.nvml()
+            if s is not None:
+                self.samples.append(s)
+
+    def _loop(self):
+        while not self.stop.is_set():
+            self.sample()
+            self.stop.wait(self.period)
+
+    # -- nvidia-smi fallback ----------------------------------------------
+    def _read_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.strip().split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm, mx = float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            try:
+                p = float(f[3])
+            except ValueError:
+                p = None
+            act = [nm for nm, v in zip(names, f[5:9]) if v.lower().startswith("active")]
+            self.samples.append((time.perf_counter(), sm, mx, p, act))
 
     def __enter__(self):
+        self.nvml = self._open_nvml()
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+            return self
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
                                           "-lms", "100", "-i", self.gpu], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
+            self.thread = threading.Thread(target=self._read_smi, daemon=True)
+            self.thread.start()
             time.sleep(0.3)
         except OSError:
             self.proc = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
+        self.stop.set()
         if self.proc is not None:
             time.sleep(0.15)
             self.proc.terminate()
@@ -132,26 +217,28 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+    def poll_until(self, event):
+        """Sample from this thread until ``event`` (recorded after the timed
+        work) has completed; the GPU is busy with the enqueued work meanwhile."""
+        while not event.query():
+            self.sample()
+            time.sleep(0.0005)
+
+    def summary(self, t0=None, t1=None):
+        sel = [s for s in self.samples if (t0 is None or s[0] >= t0) and (t1 is None or s[0] <= t1)]
+        src = "nvml" if self.nvml is not None else ("nvidia-smi" if self.proc is not None else None)
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": src,
+                    "window_s": None if t0 is None or t1 is None else t1 - t0}
+        sm = [s[1] for s in sel]
+        pw = [s[3] for s in sel if s[3] is not None]
+        reasons = sorted({r for s in sel for r in s[4]})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(s[2] for s in sel), "sm_mhz_min": min(sm),
+                "reasons": reasons, "samples": len(sel), "power_w_max": max(pw) if pw else None, "source": src,
+                "window_s": None if t0 is None or t1 is None else t1 - t0}
 
 
 def gpu_id_for_smi(dev: torch.device) -> str:
@@ -317,6 +404,7 @@ def time_device(step: DecodeStep, steps: int, warmup: int, barrier):
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(gpu_id_for_smi(step.dev)) as clk:
+        t0 = time.perf_counter()
         start.record(stream)
         for i in range(steps):
             for l in range(layers):
@@ -326,12 +414,15 @@ def time_device(step: DecodeStep, steps: int, warmup: int, barrier):
                 step.decode(l)
                 ev[i][3 * l + 2].record(stream)
         end.record(stream)
+        clk.poll_until(end)
         torch.cuda.synchronize()
+        t1 = time.perf_counter()
     barrier()
     total_ms = start.elapsed_time(end)
     dec_ms = [e[3 * l + 1].elapsed_time(e[3 * l + 2]) for e in ev for l in range(layers)]
     wr_ms = [e[3 * l].elapsed_time(e[3 * l + 1]) for e in ev for l in range(layers)]
-    return total_ms, dec_ms, wr_ms, clk.summary()
+    step_ms = [e[0].elapsed_time(e[3 * layers - 1]) for e in ev]
+    return total_ms, dec_ms, wr_ms, clk.summary(t0, t1), step_ms
 
 
 def time_device_graph(step: DecodeStep, steps: int, warmup: int, barrier):
@@ -364,14 +455,21 @@ def time_device_graph(step: DecodeStep, steps: int, warmup: int, barrier):
     barrier()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     with ClockSampler(gpu_id_for_smi(step.dev)) as clk:
+        t0 = time.perf_counter()
         start.record()
-        for _ in range(steps):
+        for i in range(steps):
+            marks[i].record()
             graph.replay()
+        marks[steps].record()
         end.record()
+        clk.poll_until(end)
         torch.cuda.synchronize()
+        t1 = time.perf_counter()
     barrier()
-    return start.elapsed_time(end), dec_eager, [], clk.summary()
+    step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(steps)]
+    return start.elapsed_time(end), dec_eager, [], clk.summary(t0, t1), step_ms
 
 
 def _blob_layout(parts):
@@ -741,6 +839,319 @@ def mixed_main(args):
 
 
 # ---------------------------------------------------------------------------
+# every workload of the scope table in the same run: one short timed block each
+# ---------------------------------------------------------------------------
+
+_T0 = time.perf_counter()
+
+
+def log(msg: str) -> None:
+    """Progress of the run on stderr (the JSON line stays alone on stdout)."""
+    print(f"[bench {time.perf_counter() - _T0:7.1f} s] {msg}", file=sys.stderr, flush=True)
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+class OmpThreads:
+    """Runs the oracle with n OpenMP threads (the oracle's libgomp), then
+    restores the default."""
+
+    def __init__(self, n: int):
+        self.n = n
+
+    def __enter__(self):
+        import ctypes
+        self.gomp = ctypes.CDLL("libgomp.so.1")
+        self.before = self.gomp.omp_get_max_threads()
+        self.gomp.omp_set_num_threads(int(self.n))
+        return self
+
+    def __exit__(self, *exc):
+        self.gomp.omp_set_num_threads(int(self.before))
+
+
+def cpu_baseline_decode(w: W.Workload, budget_s: float, budget_1core_s: float, int8: bool = False) -> dict:
+    """The binary64 oracle on the host cores, all of them and one, on a bounded
+    sample of the workload (its first sequences, host data of its shapes)."""
+    if budget_s <= 0:
+        return None
+    import oracle
+    oracle.build()
+    rate_fn = oracle_sample_rate_int8 if int8 else oracle_sample_rate
+    rate, n, dt, cores = rate_fn(w, budget_s)
+    with OmpThreads(1):
+        rate1, n1, dt1, _ = rate_fn(w, budget_1core_s)
+    kind = "int8 codes" if int8 else "K/V"
+    return {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "value_1core": rate1,
+            "cpu_model": cpu_model(),
+            "sample": f"first {n} of {w.batch} sequences ({dt:.2f} s per call); one core: first {n1} "
+                      f"({dt1:.2f} s); GB/s of algorithmic {kind} bytes, binary64 C oracle"}
+
+
+def oracle_sample_rate_int8(w: W.Workload, budget_s: float, seqs_per_call=None):
+    """oracle_sample_rate for the int8 cache: codes and per-block-per-head scales."""
+    import oracle
+    g = W.generator(w.seed + 2000)
+    rng = np.random.default_rng(w.seed + 2000)
+    cores = len(os.sched_getaffinity(0))
+    hq, hkv, d, bs = w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
+
+    def run(n):
+        lens = w.lengths[:n]
+        nb = sum(W.blocks_for(L, bs) for L in lens)
+        kq = rng.integers(-127, 128, (nb, bs, hkv, d), dtype=np.int8)
+        vq = rng.integers(-127, 128, (nb, bs, hkv, d), dtype=np.int8)
+        ks = (rng.random((nb, hkv)) * 0.03 + 0.01).astype(np.float32)
+        vs = (rng.random((nb, hkv)) * 0.03 + 0.01).astype(np.float32)
+        q = W.normal(g, (n, hq, d), w.sigma, w.dtype)
+        tables, _ = W.scattered_tables(g, lens, bs, nb)
+        t0 = time.perf_counter()
+        oracle.paged_attention_int8(q, w.dtype, kq, vq, ks, vs, tables.numpy(), np.array(lens, dtype=np.int32),
+                                    w.scale)
+        return time.perf_counter() - t0, sum(lens) * hkv * d * 2
+
+    n, dt, by = 4, 0.0, 0
+    while True:
+        dt, by = run(n)
+        if dt >= budget_s or n >= w.batch:
+            break
+        n = min(w.batch, max(n + 1, int(n * min(8.0, budget_s / max(dt, 1e-3)))))
+    return by / dt / 1e9, n, dt, cores
+
+
+def cpu_baseline_prefill(m, budget_s: float) -> dict:
+    """The binary64 oracle on the mixed step's prefill chunks (512 causal rows
+    over a 2048-token prefix each): once over all 16 chunks when the one-chunk
+    estimate fits the budget, else over as many chunks as fit; one core on a
+    slice of one chunk's rows."""
+    if budget_s <= 0:
+        return None
+    import oracle
+    oracle.build()
+    g = W.generator(5000)
+    hq, hkv, d, bs, pre, ch = m.hq, m.hkv, m.d, m.bs, m.pre, m.chunk
+    npre, nown = pre // bs, W.blocks_for(ch, bs)
+    cores = len(os.sched_getaffinity(0))
+
+    def run(nchunks, rows):
+        nb = npre + nchunks * nown
+        kc = W.normal(g, (nb, bs, hkv, d), 1.0, "f16")
+        vc = W.normal(g, (nb, bs, hkv, d), 1.0, "f16")
+        tab = np.full((nchunks, npre + nown), -1, np.int32)
+        for i in range(nchunks):
+            tab[i, :npre] = np.arange(npre)
+            tab[i, npre:] = npre + i * nown + np.arange(nown)
+        # the last `rows` rows of each chunk (the most keys)
+        lens = np.full(nchunks, pre + ch, np.int32)
+        cu = np.arange(nchunks + 1, dtype=np.int32) * rows
+        q = W.normal(g, (nchunks * rows, hq, d), 1.0, "f16")
+        t0 = time.perf_counter()
+        oracle.paged_attention(q, kc, vc, "f16", tab, lens, m.scale, cu_q=cu, causal=True)
+        flops = 4 * d * hq * nchunks * sum(pre + ch - rows + i + 1 for i in range(rows))
+        return time.perf_counter() - t0, flops
+
+    dt1, fl1 = run(1, ch)
+    k = m.nchunk if dt1 * m.nchunk * 8 / max(1, min(cores, 8 * m.nchunk)) <= budget_s else 1
+    dt, fl = (dt1, fl1) if k == 1 else run(k, ch)
+    with OmpThreads(1):
+        dt_1, fl_1 = run(1, 64)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "value_1core": fl_1 / dt_1 / 1e12, "cpu_model": cpu_model(),
+            "sample": f"{k} of {m.nchunk} chunks x {ch} causal rows ({fl / 1e9:.1f} GFLOP) in one call, "
+                      f"{dt:.1f} s; one core: the last 64 rows of one chunk ({dt_1:.1f} s); binary64 C oracle"}
+
+
+def time_parts(parts, iters, warmup, clk, before=None):
+    """CUDA-event time (ms) of each callable of ``parts`` per iteration, on the
+    current stream; ``before`` (an L2 flush) runs outside the events.  Returns
+    the [iters][parts] times and the clock summary of the timed window."""
+    for _ in range(warmup):
+        if before is not None:
+            before()
+        for f in parts:
+            f()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(iters)]
+    end = torch.cuda.Event()
+    t0 = time.perf_counter()
+    for i in range(iters):
+        if before is not None:
+            before()
+        for j, f in enumerate(parts):
+            ev[i][j].record()
+            f()
+        ev[i][-1].record()
+    end.record()
+    clk.poll_until(end)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    return [[e[j].elapsed_time(e[j + 1]) for j in range(len(parts))] for e in ev], clk.summary(t0, t1)
+
+
+def _hbm_roofline(bytes_, ms, peak, kernel):
+    a = bytes_ / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": kernel, "achieved": a, "peak": peak, "unit": "GB/s", "frac": a / peak,
+            "algorithmic_bytes_per_launch": bytes_, "launch_ms_median": ms}
+
+
+def _med(xs):
+    return statistics.median(xs)
+
+
+def config_blocks(dev, iters: int, cpu_budget_s: float) -> dict:
+    """Each workload of the scope table, timed in its own short block: median of
+    ``iters`` iterations after 10 warm-up ones, its own roofline and clock
+    window, and its own CPU oracle baseline."""
+    import gc
+    hbm, kind = measured_peak()
+    tc, tc_kind = measured_tc_peak()
+    gid = gpu_id_for_smi(dev)
+    out = {}
+    wu = 10
+    with ClockSampler(gid) as clk:
+        log("config block: 1 tiny MHA decode")
+        # 1: tiny MHA decode, latency-bound; L2 flushed before every iteration
+        w = W.tiny_decode()
+        st = DecodeStep(w, dev)
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        ms, ck = time_parts([st.write, st.decode], iters, wu, clk, before=flush.zero_)
+        dec_b, wr_b = st.bytes()
+        step = _med([a + b for a, b in ms])
+        out["tiny"] = {
+            "workload": w.name, "iters": iters, "ms_per_step": step,
+            "ms_per_step_mean": float(np.mean([a + b for a, b in ms])), "tokens_per_s": w.batch / (step * 1e-3),
+            "GB_per_s": (dec_b + wr_b) / (step * 1e-3) / 1e9, "l2": "512 MB written before every iteration",
+            "roofline": dict(_hbm_roofline(dec_b, _med([b for _, b in ms]), hbm, "pkv_attn_decode"),
+                             note="0.33 MB per call: launch- and latency-bound, not an HBM claim"),
+            "clocks": ck, "cpu_baseline": cpu_baseline_decode(w, cpu_budget_s, cpu_budget_s / 2)}
+        del st, flush
+        gc.collect()
+        torch.cuda.empty_cache()
+
+        log("config block: 2 GPT-2-shaped 12-layer step")
+        # 2: GPT-2-shaped 12-layer step, one CUDA graph per step
+        w = W.gpt2_decode()
+        st = DecodeStep(w, dev)
+        layers = w.layers
+        graph = st.P.StepGraph(lambda: [(st.write(l), st.decode(l)) for l in range(layers)])
+        dec_graph = st.P.StepGraph(lambda: [st.decode(l) for l in range(layers)])
+        ms, ck = time_parts([graph.replay], iters, wu, clk)
+        msd, _ = time_parts([dec_graph.replay], iters, wu, clk)
+        dec_b, wr_b = st.bytes()
+        step = _med([x[0] for x in ms])
+        out["gpt2"] = {
+            "workload": w.name, "iters": iters, "ms_per_step": step, "ms_per_step_mean": float(np.mean(ms)),
+            "tokens_per_s": w.batch / (step * 1e-3), "GB_per_s": layers * (dec_b + wr_b) / (step * 1e-3) / 1e9,
+            "timed_as": "one CUDA graph per 12-layer step (write + decode per layer)",
+            "l2": "12 pools, %.0f MB of K/V per step vs 129 MB of L2, no flush" % (
+                layers * sum(w.lengths) * kv_bytes_per_token(w.num_kv_heads, w.head_dim, 2) / 1e6),
+            "roofline": _hbm_roofline(dec_b, _med([x[0] for x in msd]) / layers, hbm,
+                                      "pkv_attn_decode (12 launches in one graph, per launch)"),
+            "clocks": ck, "cpu_baseline": cpu_baseline_decode(w, cpu_budget_s, cpu_budget_s / 2)}
+        del st, graph, dec_graph
+        gc.collect()
+        torch.cuda.empty_cache()
+
+        log("config block: 4 long / skewed contexts")
+        # 4: long / skewed contexts 1k .. 128k, split-K over every CTA
+        w = W.long_skewed_decode()
+        st = DecodeStep(w, dev)
+        ms, ck = time_parts([st.write, st.decode], iters, wu, clk)
+        dec_b, wr_b = st.bytes()
+        step = _med([a + b for a, b in ms])
+        out["skew"] = {
+            "workload": w.name, "iters": iters, "ms_per_step": step,
+            "ms_per_step_mean": float(np.mean([a + b for a, b in ms])), "tokens_per_s": w.batch / (step * 1e-3),
+            "GB_per_s": (dec_b + wr_b) / (step * 1e-3) / 1e9, "l2": "1.07 GB of K/V per step, no flush",
+            "roofline": _hbm_roofline(dec_b, _med([b for _, b in ms]), hbm, "pkv_attn_decode (split-K + merge)"),
+            "clocks": ck, "cpu_baseline": cpu_baseline_decode(w, cpu_budget_s, cpu_budget_s / 2)}
+        del st
+        gc.collect()
+        torch.cuda.empty_cache()
+
+        log("config block: GQA 32/8 over an int8 cache")
+        # GQA 32/8 over an int8 cache (codes + per-block-per-head scales)
+        w = W.gqa_decode()
+        st = DecodeStepInt8(w, dev)
+        ms, ck = time_parts([st.write, st.decode], iters, wu, clk)
+        dec_b, wr_b = st.bytes()
+        step = _med([a + b for a, b in ms])
+        out["gqa_int8"] = {
+            "workload": w.name + "_int8", "iters": iters, "ms_per_step": step,
+            "ms_per_step_mean": float(np.mean([a + b for a, b in ms])), "tokens_per_s": w.batch / (step * 1e-3),
+            "GB_per_s": (dec_b + wr_b) / (step * 1e-3) / 1e9, "l2": "1.21 GB of codes per step, no flush",
+            "roofline": _hbm_roofline(dec_b, _med([b for _, b in ms]), hbm, "pkv_attn_decode_int8 (split-K + merge)"),
+            "clocks": ck, "cpu_baseline": cpu_baseline_decode(w, cpu_budget_s, cpu_budget_s / 2, int8=True)}
+        del st
+        gc.collect()
+        torch.cuda.empty_cache()
+
+        log("config block: 5 mixed packed step")
+        # 5: mixed packed step (prefill chunks + decode rows), then the beam split
+        m = MixedStep(dev)
+        n_mix = max(50, iters // 2)
+        ms1, ck1 = time_parts([m.step1], n_mix, wu, clk)
+        ms2, ck2 = time_parts([m.step2], n_mix, wu, clk)
+        msp, ckp = time_parts([m.prefill_only], n_mix, wu, clk)
+        msd, ckd = time_parts([m.decode_only], n_mix, wu, clk)
+        assert int(m.err.item()) == 0, f"device error word {int(m.err.item())}"
+        fl = m.prefill_flops()
+        tp = _med([x[0] for x in msp])
+        td = _med([x[0] for x in msd])
+        a_tc = fl / (tp * 1e-3) / 1e12
+        db = m.decode_rows_bytes()
+        out["mixed"] = {
+            "workload": "mixed_prefix2048_16x512_prefill_240_decode_bs32_beam4x32", "iters": n_mix,
+            "step1_ms": _med([x[0] for x in ms1]), "step2_ms": _med([x[0] for x in ms2]),
+            "step1_rows_per_s": (m.nchunk * m.chunk + m.ndec) / (_med([x[0] for x in ms1]) * 1e-3),
+            "step2_beams": len(m.s2_lens_host), "step2_cow_pairs": m.npairs,
+            "prefill_only": {"ms": tp, "gflop": fl / 1e9, "clocks": ckp,
+                             "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05)",
+                                          "achieved": a_tc, "peak": tc, "unit": "TFLOP/s", "frac": a_tc / tc,
+                                          "peak_kind": tc_kind}},
+            "decode_rows_only": {"ms": td, "clocks": ckd,
+                                 "roofline": dict(_hbm_roofline(db, td, hbm, "pkv_attn_decode (240 rows)"),
+                                                  note="logical bytes: the 2,048-token shared prefix is re-read "
+                                                       "by every row and mostly served from L2")},
+            "clocks": {"step1": ck1, "step2": ck2},
+            "cpu_baseline": {"prefill": cpu_baseline_prefill(m, 7 * cpu_budget_s),
+                             "decode_rows": cpu_baseline_decode(
+                                 dataclasses.replace(W.gqa_decode(), name="mixed_decode_rows", lengths=list(
+                                     m.s1_lens_host[m.nchunk:]), block_size=32, num_blocks=1, seed=5),
+                                 cpu_budget_s, cpu_budget_s / 2)}}
+        del m
+        gc.collect()
+        torch.cuda.empty_cache()
+    return out
+
+
+def measured_tc_peak():
+    """Dense 16-bit tensor peak: the measured bf16 burst figure (fp16 has the
+    same nominal rate), else the fallback 1.9 PFLOP/s."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst; fp16 = bf16 nominal)"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback 1.9 PFLOP/s bf16 dense"
+
+
+# ---------------------------------------------------------------------------
 
 def main():
     ap = argparse.ArgumentParser()
@@ -760,6 +1171,10 @@ def main():
                     help="reference arm: CPU seconds the whole --steps/--warmup run is sized to")
     ap.add_argument("--batch", type=int, default=0,
                     help="use only the first N sequences (a smaller case of the same workload, for profiling)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the short timed block of every other workload (tiny, gpt2, skew, int8, mixed)")
+    ap.add_argument("--configs-iters", type=int, default=100,
+                    help="timed iterations per workload block (median reported)")
     ap.add_argument("--fused-append", action="store_true",
                     help="gqa/gpt2/skew: write the new K/V rows inside the decode kernel (pkv_attn_decode_append) "
                          "instead of pkv_write_kv then pkv_attn_decode")
@@ -803,7 +1218,9 @@ def main():
         step.fused = True
     use_graph = args.graph == "on" or (args.graph == "auto" and w.layers > 1)
     timer = time_device_graph if use_graph else time_device
-    total_ms, dec_ms, wr_ms, clocks = timer(step, args.steps, args.warmup, barrier)
+    log(f"workload {w.name} set up")
+    total_ms, dec_ms, wr_ms, clocks, step_ms = timer(step, args.steps, args.warmup, barrier)
+    log("headline timed")
     dec_b, wr_b = step.bytes()
     step_bytes = (dec_b + wr_b) * w.layers
     total_ms = max_over_ranks(total_ms, pg, dev)
@@ -822,7 +1239,8 @@ def main():
         traffic = None  # the committed capture covers the full GQA 32/8 workload, write then decode
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_median": statistics.median(step_ms),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "block_size": w.block_size, "mean_context": sum(w.lengths) / w.batch,
@@ -866,10 +1284,22 @@ def main():
                                "pkv_write_kv -> pkv_attn_decode] -> one D2H of the output -> host read; two buffer "
                                "sets: host work and both copies of neighbouring steps overlap step i's kernels",
                        "serial_ms_per_step": ser_ms / n_e2e}
+    log("e2e timed")
     if rank == 0 and not args.no_cpu_baseline:
         rate, n, dt, cores = oracle_sample_rate(w, 5.0)
+        with OmpThreads(1):
+            rate1, n1, dt1, _ = oracle_sample_rate(w, 2.0)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"first {n} of {w.batch} sequences, one call, {dt:.1f} s, binary64 C oracle"}
+                                "value_1core": rate1, "cpu_model": cpu_model(),
+                                "sample": f"first {n} of {w.batch} sequences, one call, {dt:.1f} s; one core: "
+                                          f"first {n1} ({dt1:.1f} s); binary64 C oracle"}
+    if rank == 0 and not args.no_configs and args.workload == "gqa" and not args.batch:
+        del step
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        line["configs"] = config_blocks(dev, args.configs_iters, 1.5 if not args.no_cpu_baseline else 0.0)
+    log("done")
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
