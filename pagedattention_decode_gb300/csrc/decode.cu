@@ -16,12 +16,17 @@
 //    leaves (running max, running sum, unnormalised output) records in the
 //    workspace that decode_merge_kernel combines.  Balance is exact whatever
 //    the length mix.
-//  * Data movement: one producer warp walks the block tables and issues TMA
-//    tensor loads (one 16-token x 64-dim tile, 2 KB, 128-byte swizzle, per KV
-//    head and half of head_dim) into a ring of shared-memory stages guarded by
-//    mbarriers; a stage holds K and V of 16 tokens for every KV head of the CTA.
-//    Each K/V byte is read from HBM once (GQA: the query heads of a group share
-//    it).
+//  * Data movement: one producer warp walks the block tables and issues two
+//    TMA tensor loads per 16-token sub-block, K and V, into a ring of
+//    shared-memory stages guarded by mbarriers.  Each load is one box of 16
+//    token rows x every 128-byte chunk of the CTA's KV heads (a view of the
+//    pool with the chunk dimension outside the row dimension), so it lands as
+//    one 2 KB, 128-byte-swizzled tile per (KV head, half of head_dim).  A TMA
+//    box costs ~50 cycles on the SM besides its bytes: 2 KB boxes, one per tile,
+//    held an SM near 25 B/clk (GQA decode call 6,886 GB/s, the mixed step's
+//    L2-served decode rows 0.567 ms); one box per K or V of a stage gives
+//    7,015 GB/s and 0.371 ms.  Each K/V byte is read from HBM once (GQA: the
+//    query heads of a group share it).
 //  * Math: one consumer warp per KV head.  Scores for 16 tokens x the group's
 //    query heads come from mma.sync m16n8k16 (tokens as M, heads as N, fp32
 //    accumulate); the online softmax (running max in base 2, rescaled running
@@ -407,15 +412,12 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : (D =
                             bulk_copy_g2s(ds + p.hkv, p.v_scale + (int64_t)rb * p.hkv, 4 * p.hkv, &full[stage]);
                         }
                     }
+                    // one copy for K and one for V: 16 token rows x this
+                    // CTA's `tiles` chunks, landing as `tiles` 2 KB tiles
                     uint8_t *sbase = base + stage * stage_bytes;
-                    for (int tt = lane; tt < 2 * tiles; tt += 32) {
-                        const int which = tt >= tiles;
-                        const int hh = which ? tt - tiles : tt;
-                        const int head = hg * HG + hh / HALVES;
-                        const int half = hh % HALVES;
-                        tma_load_3d(sbase + tt * kTile, which ? &tmv : &tmk, &full[stage], 0, head * HALVES + half, r,
-                                    pol);
-                    }
+                    if (lane < 2)
+                        tma_load_3d(sbase + lane * tiles * kTile, lane ? &tmv : &tmk, &full[stage], 0, r,
+                                    hg * tiles, pol);
                     ++it;
                     if (++pstage == NS) {
                         pstage = 0;
@@ -1049,9 +1051,10 @@ static pkv_status run_decode_impl(const void *q, int64_t q_stride, const pkv_cac
     PKV_CHECK_ARG((reinterpret_cast<uintptr_t>(workspace) & 255) == 0, PKV_ERR_INVALID_ARG,
                   "workspace must be 256-byte aligned");
     CUtensorMap mk, mv;
-    st = encode_pool_map(&mk, cache->k, cache);
+    const int chunks = pl.heads_per_cta * (cache->head_dim / 64);
+    st = encode_pool_rows_map(&mk, cache->k, cache, chunks);
     if (st != PKV_OK) return st;
-    st = encode_pool_map(&mv, cache->v, cache);
+    st = encode_pool_rows_map(&mv, cache->v, cache, chunks);
     if (st != PKV_OK) return st;
     DecodeParams p{};
     p.q = q;
@@ -1128,9 +1131,9 @@ static pkv_status run_decode_i8(const void *q, int64_t q_stride, const pkv_cache
     PKV_CHECK_ARG((reinterpret_cast<uintptr_t>(workspace) & 255) == 0, PKV_ERR_INVALID_ARG,
                   "workspace must be 256-byte aligned");
     CUtensorMap mk, mv;
-    st = encode_pool_map_i8(&mk, cache->k, cache);
+    st = encode_pool_rows_map_i8(&mk, cache->k, cache, pl.heads_per_cta);
     if (st != PKV_OK) return st;
-    st = encode_pool_map_i8(&mv, cache->v, cache);
+    st = encode_pool_rows_map_i8(&mv, cache->v, cache, pl.heads_per_cta);
     if (st != PKV_OK) return st;
     DecodeParams p{};
     p.q = q;

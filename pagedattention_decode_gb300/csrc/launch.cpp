@@ -92,17 +92,44 @@ pkv_status encode_pool_map(CUtensorMap *map, void *base, const pkv_cache *c, int
     return PKV_OK;
 }
 
-pkv_status encode_pool_map_i8(CUtensorMap *map, void *base, const pkv_cache_i8 *c) {
+// The pool seen as [head chunks][token rows][64 elements] (innermost last): a
+// box of 16 token rows x `chunks` consecutive 128-byte chunks (one KV head's
+// half of head_dim each) is one TMA copy that lands chunk by chunk, each as
+// 16 swizzled 128-byte lines in a 2 KB tile of its own -- the layout the
+// decode consumers read with ldmatrix.  The chunk stride (128 bytes) is
+// smaller than the row stride: the dimensions are listed in the order the
+// box is laid out in shared memory, not by stride.
+pkv_status encode_pool_rows_map(CUtensorMap *map, void *base, const pkv_cache *c, int chunks) {
     auto fn = encode_fn();
     PKV_CHECK_ARG(fn, PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    cuuint64_t dims[3] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_kv_heads,
-                          (cuuint64_t)c->num_blocks * c->block_size};
-    cuuint64_t strides[2] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_kv_heads * c->head_dim};
-    cuuint32_t box[3] = {128, 1, 16};
+    const int tiles = c->num_kv_heads * c->head_dim / 64;
+    PKV_CHECK_ARG(chunks >= 1 && chunks <= tiles && chunks <= 256, PKV_ERR_INVALID_ARG, "pool box of %d chunks",
+                  chunks);
+    cuuint64_t dims[3] = {64, (cuuint64_t)c->num_blocks * c->block_size, (cuuint64_t)tiles};
+    cuuint64_t strides[2] = {(cuuint64_t)c->num_kv_heads * c->head_dim * 2, 128};
+    cuuint32_t box[3] = {64, 16, (cuuint32_t)chunks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    PKV_CHECK_ARG(r == CUDA_SUCCESS, PKV_ERR_CUDA, "cuTensorMapEncodeTiled (pool rows) failed (%d)", (int)r);
+    return PKV_OK;
+}
+
+// The int8 pool the same way: chunks are whole KV heads (128 codes).
+pkv_status encode_pool_rows_map_i8(CUtensorMap *map, void *base, const pkv_cache_i8 *c, int heads) {
+    auto fn = encode_fn();
+    PKV_CHECK_ARG(fn, PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    PKV_CHECK_ARG(heads >= 1 && heads <= c->num_kv_heads, PKV_ERR_INVALID_ARG, "int8 pool box of %d heads", heads);
+    cuuint64_t dims[3] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_blocks * c->block_size,
+                          (cuuint64_t)c->num_kv_heads};
+    cuuint64_t strides[2] = {(cuuint64_t)c->num_kv_heads * c->head_dim, (cuuint64_t)c->head_dim};
+    cuuint32_t box[3] = {128, 16, (cuuint32_t)heads};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    PKV_CHECK_ARG(r == CUDA_SUCCESS, PKV_ERR_CUDA, "cuTensorMapEncodeTiled (int8 pool) failed (%d)", (int)r);
+    PKV_CHECK_ARG(r == CUDA_SUCCESS, PKV_ERR_CUDA, "cuTensorMapEncodeTiled (int8 pool rows) failed (%d)", (int)r);
     return PKV_OK;
 }
 

@@ -64,7 +64,9 @@ pkv_status encode_pool_map(CUtensorMap *map, void *base, const pkv_cache *c, int
 
 // The same for an int8 pool with head_dim 128: box = 16 rows x 1 head x 128
 // codes (one 2 KB shared tile per KV head per 16 tokens).
-pkv_status encode_pool_map_i8(CUtensorMap *map, void *base, const pkv_cache_i8 *c);
+// [chunks][rows][64] views: one box = 16 token rows x `chunks` 128-byte chunks
+pkv_status encode_pool_rows_map(CUtensorMap *map, void *base, const pkv_cache *c, int chunks);
+pkv_status encode_pool_rows_map_i8(CUtensorMap *map, void *base, const pkv_cache_i8 *c, int heads);
 
 // 3-D tensor map over packed query rows [total_q][Hq * D / 64][64] (row
 // stride q_stride elements), box = `rows` rows x 1 x 64 elements, 128-byte
