@@ -1051,20 +1051,29 @@ def config_blocks(dev, iters: int, cpu_budget_s: float) -> dict:
         layers = w.layers
         graph = st.P.StepGraph(lambda: [(st.write(l), st.decode(l)) for l in range(layers)])
         dec_graph = st.P.StepGraph(lambda: [st.decode(l) for l in range(layers)])
-        ms, ck = time_parts([graph.replay], iters, wu, clk)
+        # the same step with each layer's new row written by its decode kernel
+        # (pkv_attn_decode_append: one launch fewer per layer, bit-identical)
+        st.fused = True
+        graph_fused = st.P.StepGraph(lambda: [(st.write(l), st.decode(l)) for l in range(layers)])
+        st.fused = False
+        ms, ck = time_parts([graph_fused.replay], iters, wu, clk)
+        msp, _ = time_parts([graph.replay], iters, wu, clk)
         msd, _ = time_parts([dec_graph.replay], iters, wu, clk)
         dec_b, wr_b = st.bytes()
         step = _med([x[0] for x in ms])
         out["gpt2"] = {
             "workload": w.name, "iters": iters, "ms_per_step": step, "ms_per_step_mean": float(np.mean(ms)),
+            "ms_per_step_write_then_decode": _med([x[0] for x in msp]),
             "tokens_per_s": w.batch / (step * 1e-3), "GB_per_s": layers * (dec_b + wr_b) / (step * 1e-3) / 1e9,
-            "timed_as": "one CUDA graph per 12-layer step (write + decode per layer)",
+            "timed_as": "one CUDA graph per 12-layer step; each layer one pkv_attn_decode_append (the new row "
+                        "written by the decode kernel, then attended); ms_per_step_write_then_decode: pkv_write_kv "
+                        "then pkv_attn_decode per layer",
             "l2": "12 pools, %.0f MB of K/V per step vs 129 MB of L2, no flush" % (
                 layers * sum(w.lengths) * kv_bytes_per_token(w.num_kv_heads, w.head_dim, 2) / 1e6),
             "roofline": _hbm_roofline(dec_b, _med([x[0] for x in msd]) / layers, hbm,
                                       "pkv_attn_decode (12 launches in one graph, per launch)"),
             "clocks": ck, "cpu_baseline": cpu_baseline_decode(w, cpu_budget_s, cpu_budget_s / 2)}
-        del st, graph, dec_graph
+        del st, graph, dec_graph, graph_fused
         gc.collect()
         torch.cuda.empty_cache()
 

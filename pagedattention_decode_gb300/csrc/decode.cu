@@ -1012,7 +1012,13 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     static std::atomic<uint64_t> smem_set{0};
     pkv_status st = set_smem_once(reinterpret_cast<const void *>(kern), 210 * 1024, &smem_set);
     if (st != PKV_OK) return st;
-    st = launch_pdl(kern, dim3(pl.cmax, pl.num_hg), dim3(pl.threads), (size_t)pl.smem_bytes, stream, mk, mv, p);
+    // the table width bounds a head group's sub-blocks (every sequence at its
+    // table's capacity): a small call launches only the CTAs its split can use
+    // (the split itself takes min(its need, gridDim.x), so results are the same)
+    const int64_t bound = (int64_t)p.num_seqs * p.max_blocks * ((p.block_size + kSub - 1) / kSub);
+    const int64_t need = (bound + kMinSubBlocksPerCta - 1) / kMinSubBlocksPerCta;
+    const unsigned grid_x = (unsigned)(need < 1 ? 1 : need < pl.cmax ? need : pl.cmax);
+    st = launch_pdl(kern, dim3(grid_x, pl.num_hg), dim3(pl.threads), (size_t)pl.smem_bytes, stream, mk, mv, p);
     if (st != PKV_OK) return st;
     // the merge reads only what the decode kernel wrote: launch it as a
     // programmatic dependent so it is scheduled while the decode kernel drains
