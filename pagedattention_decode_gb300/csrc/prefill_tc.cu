@@ -205,10 +205,14 @@ __host__ __device__ constexpr int prefill_stages() {  // stages of the K ring an
 // Registers per thread after the warpgroups re-balance them: the producer /
 // MMA warpgroup gives registers back, the two softmax warpgroups (a whole
 // row of 128 fp32 scores each per thread) take them.  Their sum must fit the
-// launch's registers (kThreads x the kernel's count): checked on the host.
+// launch's registers (kThreads x the kernel's count, 168 x 384): checked on
+// the host.  The spills sit in the producer / MMA warps, not in the softmax
+// (ptxas, head_dim 128 fp16: 148 bytes of spill loads at 72 / 216, 72 at
+// 88 / 208; the softmax starts to spill at 200): 88 / 208 took the mixed
+// step's prefill chunks from 1,075 to 1,121 TFLOP/s (A/B on one box).
 constexpr int kThreads = 384;
-constexpr int kRegsLow = 72;
-constexpr int kRegsHigh = 216;
+constexpr int kRegsLow = 88;
+constexpr int kRegsHigh = 208;
 constexpr int kRegsAtLaunchMin = (128 * kRegsLow + 256 * kRegsHigh + kThreads - 1) / kThreads;
 // Epilogue staging: each softmax warp passes 16 columns of its 32 O rows
 // through shared memory (row stride 20 floats: conflict-free 16-byte
