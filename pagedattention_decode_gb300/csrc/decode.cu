@@ -884,6 +884,11 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     constexpr int OUTS = kMergeHeads * D / 4;          // float4 outputs of a full head group
     constexpr int GROUPS = kMergeThreads / OUTS;        // part groups
     float *s_w = reinterpret_cast<float *>(s_merge + GROUPS * OUTS);
+    // thread = (part group, output); its first part's output is loaded now, beside the weights' loads
+    const int o = threadIdx.x % OUTS, grp = threadIdx.x / OUTS;
+    const int hl = o / (D / 4), d4 = o - hl * (D / 4);
+    float4 first = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (hl < nh && grp < parts) first = *reinterpret_cast<const float4 *>(p.ws_o + record(c0 + grp, h0 + hl) * D + 4 * d4);
     // weights: one warp per head, lanes over the parts
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp < nh) {
@@ -905,15 +910,20 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
         for (int c = lane; c < parts; c += 32) s_w[c * kMergeHeads + warp] *= inv;
     }
     __syncthreads();
-    // partial sums: thread = (part group, output)
-    const int o = threadIdx.x % OUTS, grp = threadIdx.x / OUTS;
-    const int hl = o / (D / 4), d4 = o - hl * (D / 4);
     float4 acc[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (hl < nh) {
         const int h = h0 + hl;
         int c = grp;
+        if (c < parts) {
+            const float w = s_w[c * kMergeHeads + hl];
+            acc[0].x += w * first.x;
+            acc[0].y += w * first.y;
+            acc[0].z += w * first.z;
+            acc[0].w += w * first.w;
+            c += GROUPS;
+        }
         for (; c + 3 * GROUPS < parts; c += 4 * GROUPS) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
