@@ -133,6 +133,32 @@ pkv_status encode_pool_rows_map_i8(CUtensorMap *map, void *base, const pkv_cache
     return PKV_OK;
 }
 
+// Packed output rows [total_q][Hq][D] seen as [heads][rows][D] (innermost
+// last): a box of `cols` elements (64 bytes) x `rows` consecutive rows x
+// `heads` consecutive heads is the part of a q tile one warp holds, staged
+// in shared memory with the 64-byte swizzle.  The head stride is smaller than
+// the row stride: the dimensions follow the order the box has in shared
+// memory.
+pkv_status encode_out_map(CUtensorMap *map, void *out, int total_q, int hq, int d, int out_dtype, int cols, int rows,
+                          int heads) {
+    auto fn = encode_fn();
+    PKV_CHECK_ARG(fn, PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const int esz = out_dtype == PKV_F32 ? 4 : 2;
+    PKV_CHECK_ARG(cols * esz == 64 && rows >= 1 && rows <= 256 && heads >= 1 && heads <= hq, PKV_ERR_INVALID_ARG,
+                  "output box %d x %d x %d", cols, rows, heads);
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)total_q, (cuuint64_t)hq};
+    cuuint64_t strides[2] = {(cuuint64_t)hq * d * esz, (cuuint64_t)d * esz};
+    cuuint32_t box[3] = {(cuuint32_t)cols, (cuuint32_t)rows, (cuuint32_t)heads};
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt = out_dtype == PKV_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : out_dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = fn(map, dt, 3, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    PKV_CHECK_ARG(r == CUDA_SUCCESS, PKV_ERR_CUDA, "cuTensorMapEncodeTiled (output rows) failed (%d)", (int)r);
+    return PKV_OK;
+}
+
 pkv_status encode_q_map(CUtensorMap *map, const void *q, int64_t q_stride, int total_q, int hq, int d, int rows,
                         int dtype) {
     auto fn = encode_fn();

@@ -66,6 +66,9 @@ pkv_status encode_pool_map(CUtensorMap *map, void *base, const pkv_cache *c, int
 // codes (one 2 KB shared tile per KV head per 16 tokens).
 // [chunks][rows][64] views: one box = 16 token rows x `chunks` 128-byte chunks
 pkv_status encode_pool_rows_map(CUtensorMap *map, void *base, const pkv_cache *c, int chunks);
+// [heads][rows][D] view of packed output rows: one box = 64 bytes x rows x heads
+pkv_status encode_out_map(CUtensorMap *map, void *out, int total_q, int hq, int d, int out_dtype, int cols, int rows,
+                          int heads);
 pkv_status encode_pool_rows_map_i8(CUtensorMap *map, void *base, const pkv_cache_i8 *c, int heads);
 
 // 3-D tensor map over packed query rows [total_q][Hq * D / 64][64] (row

@@ -43,6 +43,8 @@
 // (warps 0-3) to the two softmax warpgroups.
 #include <cuda.h>
 
+#include <cstring>
+
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -80,6 +82,7 @@ struct TcParams {
     int32_t window;   // > 0: each row attends only its most recent `window` keys
     int32_t box_rows; // rows per K/V TMA box: 128, 64, 32 or 16, a divisor of block_size
     int32_t num_seqs;
+    int32_t out_tma;  // the output map is valid: whole warps' rows leave by TMA stores
 };
 
 // UMMA shared-memory descriptor, 128-byte swizzle (sm_100 family layout:
@@ -192,6 +195,24 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
     return v;
 }
 
+// Tensor store of a shared-memory box (64-byte swizzle) into the output rows,
+// tracked in this thread's bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// This thread's earlier bulk stores have read their shared memory ...
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... or have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_u4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -232,7 +253,8 @@ struct TcItem {
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                      const __grid_constant__ CUtensorMap tmv, const TcParams p) {
+                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+                      const TcParams p) {
     constexpr int HALVES = D / 64;
     constexpr int S = prefill_stages<D>();
     constexpr int QHALF = 128 * 128;            // bytes of 128 rows x 64 dims
@@ -782,6 +804,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // shared-window address: the staging accesses are issued as
                 // shared-memory instructions, not generic ones
                 const uint32_t stg = smem_u32(stage_o) + (uint32_t)((warp - 4) * 32 * kStageStride * 4);
+                // The warp's 32 rows are min(32, R) consecutive positions of 32 / min(32, R)
+                // consecutive heads.  When all of them lie inside the chunk they leave by
+                // tensor stores: 64 bytes of each row at a time into the warp's staging
+                // rows (a 64-byte-swizzled box, 512-byte aligned: chunk k of row r at
+                // k ^ ((r >> 1) & 3), conflict-free), then one store issued by one lane
+                // while the warp goes on.  The epilogue had been ~9k cycles of every
+                // item's critical path (clock trace).
+                const int q_first = item.q00 + u * R;
+                const int wp0 = (qw * 32) % R, wpos = R < 32 ? R : 32;
+                if (p.out_tma && q_first + wp0 + wpos <= item.q_len) {
+                    const int pos0 = item.q_begin + q_first + wp0, head0 = item.kvh * G + (qw * 32) / R;
+                    const uint32_t myrow = stg + (uint32_t)lane * 64u;
+                    const uint32_t sw = (uint32_t)(lane >> 1) & 3u;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t orr[32];
+                        tmem_ld32(trow_addr + 128 + c0, orr);
+                        tmem_wait_ld();
+                        if (p.out_f32) {
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                if (lane == 0) bulk_wait_read();  // the previous store has read the rows
+                                __syncwarp();
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    const int c = h * 16 + k * 4;
+                                    st_shared_f4(myrow + (((uint32_t)k ^ sw) << 4), __uint_as_float(orr[c]) * inv,
+                                                 __uint_as_float(orr[c + 1]) * inv, __uint_as_float(orr[c + 2]) * inv,
+                                                 __uint_as_float(orr[c + 3]) * inv);
+                                }
+                                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                                __syncwarp();
+                                if (lane == 0) tma_store_3d(&tmo, stg, c0 + h * 16, pos0, head0);
+                            }
+                        } else {
+                            if (lane == 0) bulk_wait_read();
+                            __syncwarp();
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const int c = k * 8;
+                                st_shared_u4(myrow + (((uint32_t)k ^ sw) << 4),
+                                             pack2<T>(__uint_as_float(orr[c]) * inv, __uint_as_float(orr[c + 1]) * inv),
+                                             pack2<T>(__uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv),
+                                             pack2<T>(__uint_as_float(orr[c + 4]) * inv, __uint_as_float(orr[c + 5]) * inv),
+                                             pack2<T>(__uint_as_float(orr[c + 6]) * inv, __uint_as_float(orr[c + 7]) * inv));
+                            }
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                            __syncwarp();
+                            if (lane == 0) tma_store_3d(&tmo, stg, c0, pos0, head0);
+                        }
+                    }
+                } else {
+                if (lane == 0) bulk_wait_read();  // the rows may still be read by an earlier tensor store
+                __syncwarp();
                 const int rr = lane >> 2, c4 = lane & 3;
                 // the output rows this lane stores: rows k * 8 + rr of the warp
                 int64_t row_off[4];
@@ -832,6 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __syncwarp();
                     }
                 }
+                }
                 // O of this tile has been read: the next item's first P V (which
                 // overwrites O) waits for this warp's next arrival on p_full
                 tc_fence_before();
@@ -845,6 +922,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_abort = 1;
             set_err(p.err, PKV_DEVERR_TIMEOUT);
         }
+        // the output rows this warp handed to tensor stores are written before the CTA leaves
+        if (lane == 0) bulk_wait_all();
     }
 
     // ---- teardown ----
@@ -865,7 +944,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, typename T>
 static pkv_status launch_prefill_tc_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                                      const TcParams &p, int num_seqs, cudaStream_t stream) {
+                                      const CUtensorMap &mo, const TcParams &p, int num_seqs, cudaStream_t stream) {
     constexpr int HALVES = D / 64;
     // Q of both tiles + the K and V rings, + 1 KB for the 1024-byte alignment
     // of the swizzled tiles, + 4 KB of slack after the last stage, + the
@@ -892,7 +971,7 @@ static pkv_status launch_prefill_tc_t(const CUtensorMap &mq, const CUtensorMap &
     }
     PKV_CHECK_ARG(regs.load() >= kRegsAtLaunchMin, PKV_ERR_UNSUPPORTED,
                   "prefill kernel built with %d registers per thread, needs >= %d", regs.load(), kRegsAtLaunchMin);
-    return launch_pdl(kern, grid, dim3(kThreads), (size_t)smem, stream, mq, mk, mv, p);
+    return launch_pdl(kern, grid, dim3(kThreads), (size_t)smem, stream, mq, mk, mv, mo, p);
 }
 
 // Prefill chunks of a varlen call on tcgen05 (rows of q_len == 1 are left to the decode kernel).
@@ -933,12 +1012,24 @@ pkv_status run_prefill_tc(const void *q, int64_t q_stride, const pkv_cache *cach
     if (st != PKV_OK) return st;
     st = encode_pool_map(&mv, cache->v, cache, p.box_rows);
     if (st != PKV_OK) return st;
+    // output rows by tensor stores: a warp's 32 rows are min(32, 128 / G) positions of
+    // 32 / min(32, 128 / G) heads (the output must be 16-byte aligned; out is contiguous)
+    CUtensorMap mo;
+    memset(&mo, 0, sizeof(mo));
+    const int wrows = rows < 32 ? rows : 32;
+    p.out_tma = 0;
+    if (aligned16(out)) {
+        st = encode_out_map(&mo, out, total_q, num_q_heads, cache->head_dim, out_dtype, out_dtype == PKV_F32 ? 16 : 32,
+                            wrows, 32 / wrows);
+        if (st != PKV_OK) return st;
+        p.out_tma = 1;
+    }
     const bool bf = cache->dtype == PKV_BF16;
     if (cache->head_dim == 64)
-        return bf ? launch_prefill_tc_t<64, __nv_bfloat16>(mq, mk, mv, p, num_seqs, stream)
-                  : launch_prefill_tc_t<64, __half>(mq, mk, mv, p, num_seqs, stream);
-    return bf ? launch_prefill_tc_t<128, __nv_bfloat16>(mq, mk, mv, p, num_seqs, stream)
-              : launch_prefill_tc_t<128, __half>(mq, mk, mv, p, num_seqs, stream);
+        return bf ? launch_prefill_tc_t<64, __nv_bfloat16>(mq, mk, mv, mo, p, num_seqs, stream)
+                  : launch_prefill_tc_t<64, __half>(mq, mk, mv, mo, p, num_seqs, stream);
+    return bf ? launch_prefill_tc_t<128, __nv_bfloat16>(mq, mk, mv, mo, p, num_seqs, stream)
+              : launch_prefill_tc_t<128, __half>(mq, mk, mv, mo, p, num_seqs, stream);
 }
 
 }  // namespace pkv
