@@ -563,12 +563,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait(q_full, it & 1) && wait(&k_full[gc % S], (gc / S) & 1);
             if (!ok) break;
             tc_fence_after();
-            for (int u = 0; u < kTiles && ok; ++u) {
-                if (steps_of(u) == 0) continue;
+#pragma unroll
+            for (int u = 0; u < kTiles; ++u) {
+                if (!ok || steps_of(u) == 0) continue;
                 // the scores overwrite the tile's last P of the previous item
                 if (tb[u] > 0) {
                     ok = wait(o_done(u), (tb[u] - 1) & 1);
-                    if (!ok) break;
+                    if (!ok) continue;
                     tc_fence_after();
                 }
                 issue_s(u, gc);
@@ -579,29 +580,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < nt && ok; ++j) {
                 const int g = gc + j;
                 const int j1 = j + 1;
-                bool v_ready = false, k_ready = false;
-                for (int u = 0; u < kTiles && ok; ++u) {
-                    if (j >= steps_of(u)) continue;
+                const bool last_partial = (item.j_first + j1) * kTok > item.kv_len;
+                // V of the step is tested before P (it has mostly landed long before):
+                // once P arrives, only its own wait stands before the P V issue
+                ok = wait(&v_full[g % S], (g / S) & 1);
+                bool k_ready = false;
+#pragma unroll
+                for (int u = 0; u < kTiles; ++u) {
+                    if (!ok || j >= steps_of(u)) continue;
                     const uint32_t ph = (uint32_t)(tb[u] + j) & 1;
                     ok = wait(p_full(u), ph);
                     // the last step's V rows past kv_len are cleared by tile zt
-                    if (ok && u != zt && (item.j_first + j1) * kTok > item.kv_len)
-                        ok = wait(p_full(zt), (uint32_t)(tb[zt] + j) & 1);
-                    if (ok && !v_ready) ok = v_ready = wait(&v_full[g % S], (g / S) & 1);
-                    if (!ok) break;
+                    if (ok && u != zt && last_partial) ok = wait(p_full(zt), (uint32_t)(tb[zt] + j) & 1);
+                    if (!ok) continue;
                     tc_fence_after();
                     issue_pv(u, g, j == 0);
+                    // every P V that reads the stage's V issued: its release is committed
+                    // here, in the shadow of the next wait
+                    if (u == kTiles - 1 || j >= nt1) umma_commit(&v_empty[g % S]);
                     if (j1 < steps_of(u)) {
                         if (!k_ready) ok = k_ready = wait(&k_full[(g + 1) % S], ((g + 1) / S) & 1);
                         // the scores overwrite P of step j: its P V must have completed
                         if (ok) ok = wait(o_done(u), ph);
-                        if (!ok) break;
+                        if (!ok) continue;
                         tc_fence_after();
                         issue_s(u, g + 1);
                     }
                 }
                 if (!ok) break;
-                umma_commit(&v_empty[g % S]);
                 if (k_ready) umma_commit(&k_empty[(g + 1) % S]);
                 if (j1 == nt - 1) umma_commit(q_empty);  // every score MMA of the item issued
             }
