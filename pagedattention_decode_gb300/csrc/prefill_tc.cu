@@ -227,10 +227,11 @@ __host__ __device__ constexpr int prefill_stages() {  // stages of the K ring an
 // MMA warpgroup gives registers back, the two softmax warpgroups (a whole
 // row of 128 fp32 scores each per thread) take them.  Their sum must fit the
 // launch's registers (kThreads x the kernel's count, 168 x 384): checked on
-// the host.  The spills sit in the producer / MMA warps, not in the softmax
-// (ptxas, head_dim 128 fp16: 148 bytes of spill loads at 72 / 216, 72 at
-// 88 / 208; the softmax starts to spill at 200): 88 / 208 took the mixed
-// step's prefill chunks from 1,075 to 1,121 TFLOP/s (A/B on one box).
+// the host.  ptxas, head_dim 128 fp16, with each role's code compiled alone:
+// at 88 / 208 the producer and MMA warps fit without spills and the softmax
+// warps spill 72 bytes (loads) in their step loop; at 72 / 216 the producer
+// and MMA warps spill 96 bytes and the softmax 28 more.  88 / 208 took the
+// mixed step's prefill chunks from 1,075 to 1,121 TFLOP/s (A/B on one box).
 constexpr int kThreads = 384;
 constexpr int kRegsLow = 88;
 constexpr int kRegsHigh = 208;
