@@ -22,7 +22,8 @@ table, each in a short block of its own (median of 100 iterations, 50 for the
 mixed step), with its roofline, the clocks sampled inside its timed window
 and its CPU oracle baseline (all cores and one core): the tiny MHA decode,
 the GPT-2-shaped 12-layer step, the long/skewed contexts, the GQA step over an
-int8 cache, and the mixed packed step (prefill chunks + decode rows, then a
+int8 cache, the GQA step with a 1,024-token sliding window, and the mixed
+packed step (prefill chunks + decode rows, then a
 width-4 beam split with copy-on-write).  Clocks come from NVML (read only)
 sampled every few ms and while the GPU drains the enqueued work.
 
@@ -98,6 +99,11 @@ def decode_bytes(lengths, hq, hkv, d, dtype_bytes, out_bytes, ctas_max, num_hg=1
     part = 2 * recs * (hq // num_hg) * (d + 2) * 4
     tables = sum(-(-L // 16) for L in lengths) * 4 + len(lengths) * 4
     return kv + qb + ob + part + tables
+
+
+def windowed(lengths, window):
+    """Keys each sequence attends: all of them, or its last ``window``."""
+    return [min(L, window) for L in lengths] if window > 0 else list(lengths)
 
 
 def write_bytes(tokens, hkv, d, dtype_bytes):
@@ -326,6 +332,8 @@ class DecodeStep:
 
     # fused: the new rows are written by the decode kernel (pkv_attn_decode_append)
     fused = False
+    # window > 0: each sequence attends its most recent `window` keys (pkv_attn_decode_window)
+    window = 0
 
     def write(self, layer=0):
         if self.fused:
@@ -335,12 +343,14 @@ class DecodeStep:
     def decode(self, layer=0):
         extra = dict(k_new=self.k_new, v_new=self.v_new) if self.fused else {}
         self.P.attn_decode(self.q, self.k_caches[layer], self.v_caches[layer], self.tables, self.lens, self.w.scale,
-                           out=self.out, workspace=self.ws, err=self.err, **extra)
+                           out=self.out, workspace=self.ws, err=self.err, window=self.window, **extra)
 
     def bytes(self):
-        """(decode bytes, write bytes) of one layer."""
+        """(decode bytes, write bytes) of one layer (a window counts the keys it
+        keeps)."""
         w = self.w
-        dec = decode_bytes(w.lengths, w.num_q_heads, w.num_kv_heads, w.head_dim, 2, 4, self.sms, self.num_hg)
+        dec = decode_bytes(windowed(w.lengths, self.window), w.num_q_heads, w.num_kv_heads, w.head_dim, 2, 4,
+                           self.sms, self.num_hg)
         return dec, write_bytes(w.batch, w.num_kv_heads, w.head_dim, 2)
 
 
@@ -609,10 +619,11 @@ def time_e2e(w: W.Workload, step: DecodeStep, steps: int, warmup: int, barrier, 
 # the oracle on the host cores (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample_rate(w: W.Workload, budget_s: float, seqs_per_call=None):
+def oracle_sample_rate(w: W.Workload, budget_s: float, seqs_per_call=None, window: int = 0):
     """Times the binary64 oracle on a bounded sample of the workload (the first
     sequences, their blocks generated on the host with the workload's seed and
-    shapes).  Returns (GB/s of algorithmic KV bytes, seqs, seconds, cores)."""
+    shapes; window > 0: each sequence's last ``window`` keys).  Returns (GB/s
+    of algorithmic KV bytes, seqs, seconds, cores)."""
     import oracle
     g = W.generator(w.seed + 1000)
     cores = len(os.sched_getaffinity(0))
@@ -626,8 +637,9 @@ def oracle_sample_rate(w: W.Workload, budget_s: float, seqs_per_call=None):
         q = W.normal(g, (n, hq, d), w.sigma, w.dtype)
         tables, _ = W.scattered_tables(g, lens, bs, nb)
         t0 = time.perf_counter()
-        oracle.paged_attention(q, kc, vc, w.dtype, tables.numpy(), np.array(lens, dtype=np.int32), w.scale)
-        return time.perf_counter() - t0, sum(lens) * kv_bytes_per_token(hkv, d, 2)
+        oracle.paged_attention(q, kc, vc, w.dtype, tables.numpy(), np.array(lens, dtype=np.int32), w.scale,
+                               window=window)
+        return time.perf_counter() - t0, sum(windowed(lens, window)) * kv_bytes_per_token(hkv, d, 2)
 
     oracle.build()
     if seqs_per_call is not None:
@@ -886,14 +898,19 @@ class OmpThreads:
         self.gomp.omp_set_num_threads(int(self.before))
 
 
-def cpu_baseline_decode(w: W.Workload, budget_s: float, budget_1core_s: float, int8: bool = False) -> dict:
+def cpu_baseline_decode(w: W.Workload, budget_s: float, budget_1core_s: float, int8: bool = False,
+                        window: int = 0) -> dict:
     """The binary64 oracle on the host cores, all of them and one, on a bounded
     sample of the workload (its first sequences, host data of its shapes)."""
     if budget_s <= 0:
         return None
     import oracle
     oracle.build()
-    rate_fn = oracle_sample_rate_int8 if int8 else oracle_sample_rate
+    if int8:
+        rate_fn = oracle_sample_rate_int8
+    else:
+        def rate_fn(w_, b_):
+            return oracle_sample_rate(w_, b_, window=window)
     rate, n, dt, cores = rate_fn(w, budget_s)
     with OmpThreads(1):
         rate1, n1, dt1, _ = rate_fn(w, budget_1core_s)
@@ -1107,6 +1124,27 @@ def config_blocks(dev, iters: int, cpu_budget_s: float) -> dict:
             "GB_per_s": (dec_b + wr_b) / (step * 1e-3) / 1e9, "l2": "1.21 GB of codes per step, no flush",
             "roofline": _hbm_roofline(dec_b, _med([b for _, b in ms]), hbm, "pkv_attn_decode_int8 (split-K + merge)"),
             "clocks": ck, "cpu_baseline": cpu_baseline_decode(w, cpu_budget_s, cpu_budget_s / 2, int8=True)}
+        del st
+        gc.collect()
+        torch.cuda.empty_cache()
+
+        log("config block: GQA 32/8 with a sliding window")
+        # GQA 32/8 with a 1,024-token window: each sequence reads only the
+        # sub-blocks that cover its last 1,024 keys
+        w = W.gqa_decode()
+        st = DecodeStep(w, dev)
+        st.window = 1024
+        ms, ck = time_parts([st.write, st.decode], iters, wu, clk)
+        dec_b, wr_b = st.bytes()
+        step = _med([a + b for a, b in ms])
+        kept = sum(windowed(w.lengths, st.window)) * kv_bytes_per_token(w.num_kv_heads, w.head_dim, 2)
+        out["window"] = {
+            "workload": w.name + "_window1024", "iters": iters, "window": st.window, "ms_per_step": step,
+            "ms_per_step_mean": float(np.mean([a + b for a, b in ms])), "tokens_per_s": w.batch / (step * 1e-3),
+            "GB_per_s": (dec_b + wr_b) / (step * 1e-3) / 1e9,
+            "l2": "%.2f GB of K/V in the windows per step, no flush" % (kept / 1e9),
+            "roofline": _hbm_roofline(dec_b, _med([b for _, b in ms]), hbm, "pkv_attn_decode_window (split-K + merge)"),
+            "clocks": ck, "cpu_baseline": cpu_baseline_decode(w, cpu_budget_s, cpu_budget_s / 2, window=st.window)}
         del st
         gc.collect()
         torch.cuda.empty_cache()

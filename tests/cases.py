@@ -135,12 +135,13 @@ class Subset:
         if loc:
             oracle.copy_blocks(self.k, self.v, loc)
 
-    def attend(self, q_rows, table_rows, lens, scale, dtype, cu_q=None):
+    def attend(self, q_rows, table_rows, lens, scale, dtype, cu_q=None, window=0):
         """Binary64 attention over the host copy: one row per sequence, or
-        packed causal rows when cu_q is given."""
+        packed causal rows when cu_q is given; window > 0 keeps each row's most
+        recent ``window`` keys."""
         mb = max(len(t) for t in table_rows)
         tab = np.full((len(table_rows), mb), -1, dtype=np.int32)
         for i, t in enumerate(table_rows):
             tab[i, :len(t)] = t
         return oracle.paged_attention(q_rows, self.k, self.v, dtype, tab, np.array(lens, dtype=np.int32), scale,
-                                      cu_q=cu_q, causal=cu_q is not None)
+                                      cu_q=cu_q, causal=cu_q is not None, window=window)

@@ -173,6 +173,31 @@ def test_full_size_workload_every_sequence(wl):
     assert_close(out, want, what=w.name)
 
 
+def test_full_size_window_every_sequence():
+    """The GQA 32/8 workload (256 sequences of 512-4096 tokens) with a
+    1,024-token window, launched as the bench's window block launches it:
+    every sequence against the oracle (sequences shorter than the window see
+    all their keys; the others start mid-block)."""
+    w = W.gqa_decode()
+    window = 1024
+    dev = "cuda"
+    kc = W.normal_device(w.seed * 10 + 1, (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim), w.sigma,
+                         w.dtype, dev)
+    vc = W.normal_device(w.seed * 10 + 2, kc.shape, w.sigma, w.dtype, dev)
+    g = W.generator(w.seed)
+    q = W.normal(g, (w.batch, w.num_q_heads, w.head_dim), w.sigma, w.dtype)
+    tables, _ = W.scattered_tables(g, w.lengths, w.block_size, w.num_blocks)
+    lens = torch.tensor(w.lengths, dtype=torch.int32)
+    assert min(w.lengths) < window < max(w.lengths)
+    rows = [tables[i].tolist() for i in range(w.batch)]
+    sub = Subset(kc, vc, rows)   # before any kernel of ours runs
+    out = P.attn_decode(q.to(dev), kc, vc, tables.to(dev), lens.to(dev), w.scale, window=window)
+    torch.cuda.synchronize()
+    del kc, vc
+    want = sub.attend(q, [sub.table(r) for r in rows], w.lengths, w.scale, w.dtype, window=window)
+    assert_close(out, want, what=f"{w.name} window {window}")
+
+
 @pytest.mark.parametrize("window", [1, 15, 16, 17, 100, 4096])
 @pytest.mark.parametrize("hq,hkv,d,bs,dtype", [(32, 8, 128, 16, "f16"), (12, 12, 64, 32, "bf16")])
 def test_sliding_window_decode(window, hq, hkv, d, bs, dtype):
