@@ -37,7 +37,8 @@
 //    max comes from the row's first tile with a visible key and is moved only
 //    when a step's p could pass 2^15 (their sum tells, so no per-step max is
 //    taken): then that row of O is rescaled in TMEM and P written again.  The
-//    final O row is divided by the sum and stored through shared memory.
+//    final O row is divided by the sum and leaves by TMA tensor stores from a
+//    shared-memory staging slot (rows of a ragged last tile: plain stores).
 // All 512 TMEM columns (per tile: S/P 128, O head_dim) and ~217 KB of shared
 // memory; setmaxnreg moves registers from the producer / MMA warpgroup
 // (warps 0-3) to the two softmax warpgroups.
