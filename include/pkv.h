@@ -211,6 +211,7 @@ PKV_API pkv_status pkv_attn_decode_noalloc(const void *q, int64_t q_token_stride
  *
  *   q             device [total_q, num_q_heads, head_dim], row r at r * q_token_stride;
  *                 when max_q_len > 1, q and its row stride must be 16-byte aligned.
+ *                 total_q == 0 (every row set empty) is a no-op; q and out may be NULL.
  *   cu_seqlens_q  device int32 [num_seqs + 1], nondecreasing, cu[0] = 0, cu[num_seqs] = total_q.
  *   max_q_len     host upper bound on any q_len (sizes the tile grid).
  *   out           device [total_q, num_q_heads, head_dim] of out_dtype.

@@ -54,10 +54,12 @@ static pkv_status varlen_impl(const void *q, int64_t q_token_stride, const pkv_c
                               int32_t num_q_heads, float scale, int32_t causal, int32_t window, void *out,
                               int32_t out_dtype, void *workspace, size_t workspace_bytes, int32_t *err_word,
                               pkv_stream stream, const char *what) {
-    pkv_status st = check_attention_common(q, q_token_stride, cache, block_tables, max_blocks_per_seq, seq_lens,
-                                           num_seqs, num_q_heads, out, out_dtype, what);
-    if (st != PKV_OK) return st;
     PKV_CHECK_ARG(total_q >= 0 && max_q_len >= 0, PKV_ERR_INVALID_ARG, "negative total_q or max_q_len");
+    // with no query rows (total_q == 0: every sequence's row set is empty) q and
+    // out hold nothing and may be NULL; the call does nothing
+    pkv_status st = check_attention_common(q, q_token_stride, cache, block_tables, max_blocks_per_seq, seq_lens,
+                                           total_q > 0 ? num_seqs : 0, num_q_heads, out, out_dtype, what);
+    if (st != PKV_OK) return st;
     if (num_seqs == 0 || total_q == 0) return ok();
     PKV_CHECK_ARG(cu_seqlens_q, PKV_ERR_INVALID_ARG, "cu_seqlens_q is NULL");
     PKV_CHECK_ARG(num_seqs <= 65535, PKV_ERR_UNSUPPORTED, "at most 65535 sequences per call");

@@ -147,6 +147,23 @@ def test_gqa_mapping_contiguous_groups():
     assert torch.allclose(got[0].cpu(), want, atol=1e-6)
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (12, 12, 64)])
+@pytest.mark.parametrize("window", [0, 16])
+def test_every_sequence_empty(hq, hkv, d, window):
+    """A batch whose sequences all have length 0: there is nothing to split,
+    every output row is zero, nothing is flagged, and the pool (NaN in every
+    slot, since no sequence holds one) is never read."""
+    case = decode_case(91 + d, [0, 0, 0, 0, 0], hq, hkv, d, 16, "f16")
+    assert torch.isnan(case.k_cache.float()).all()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    c = case.to("cuda")
+    got = P.attn_decode(c.q, c.k_cache, c.v_cache, c.tables, c.lens, c.scale, window=window, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_close(got, case.oracle(), what="every sequence empty")
+    assert torch.all(got == 0)
+
+
 @pytest.mark.parametrize("wl", [W.gqa_decode, W.long_skewed_decode])
 def test_full_size_workload_every_sequence(wl):
     """The full-size workloads, launched as the bench launches them; every

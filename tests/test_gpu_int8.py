@@ -82,6 +82,21 @@ def test_int8_decode_matches_oracle(hq, hkv, bs, dtype, window):
     assert_close(out, want, what=f"int8 {hq}/{hkv}/{bs}/{dtype}/w{window}")
 
 
+def test_int8_decode_every_sequence_empty():
+    """Every sequence of length 0 over an int8 pool: zero rows, nothing flagged."""
+    lens = [0, 0, 0]
+    q, kq, vq, ks, vs, tables, L = _int8_case(610, lens, 32, 8, 16, "f16")
+    dk, dv, dks, dvs = _dev(kq, vq, ks, vs)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = P.attn_decode_int8(q.cuda(), dk, dv, dks, dvs, torch.from_numpy(tables).cuda(), torch.from_numpy(L).cuda(),
+                             128 ** -0.5, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want = oracle.paged_attention_int8(q, "f16", kq, vq, ks, vs, tables, L, 128 ** -0.5)
+    assert_close(out, want, what="int8 every sequence empty")
+    assert torch.all(out == 0)
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_int8_decode_rising_and_jumping_scores(dtype):
     """Key scales that grow block by block, so the scores keep rising along

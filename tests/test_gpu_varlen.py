@@ -59,6 +59,30 @@ def test_16bit_output_varlen():
     assert_close(got, case.oracle())
 
 
+@pytest.mark.parametrize("q_lens", [[0, 0, 0], []])
+def test_no_query_rows_is_a_no_op(q_lens):
+    """total_q = 0 (every sequence's row set empty) or no sequences at all:
+    the call succeeds, returns an empty output and flags nothing."""
+    kv_lens = [5, 0, 70][:len(q_lens)]
+    if q_lens:
+        case = varlen_case(46, q_lens, kv_lens, 8, 2, 64, 16)
+        c = case.to("cuda")
+        q, kc, vc, tab, cu, lens = c.q, c.k_cache, c.v_cache, c.tables, c.cu_q, c.lens
+    else:
+        kc = torch.zeros((4, 16, 2, 64), dtype=torch.float16, device="cuda")
+        vc = torch.zeros_like(kc)
+        q = torch.empty((0, 8, 64), dtype=torch.float16, device="cuda")
+        tab = torch.zeros((0, 1), dtype=torch.int32, device="cuda")
+        cu = torch.zeros(1, dtype=torch.int32, device="cuda")
+        lens = torch.zeros(0, dtype=torch.int32, device="cuda")
+    assert q.shape[0] == 0
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = P.attn_varlen(q, kc, vc, tab, cu, lens, 0, 0.125, err=err)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 8, 64)
+    assert int(err.item()) == 0
+
+
 def test_q_len_beyond_kv_len_is_flagged():
     case = varlen_case(44, [40, 1], [30, 20], 8, 2, 64, 16)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
