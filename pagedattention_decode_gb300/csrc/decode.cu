@@ -89,7 +89,8 @@ struct DecodeParams {
     float *ws_o;                   // [num_hg][cmax][2][heads_per_cta * group][D]
     float *ws_ml;                  // [num_hg][cmax][2][heads_per_cta * group][2]
     int32_t *ws_meta;              // [0] total sub-blocks, [1] CTAs used, [2 + s] first sub-block of s
-    int32_t cmax;                  // gridDim.x
+    int32_t cmax;                  // gridDim.x at most (the records' CTA stride)
+    int32_t grid_x;                // the decode launch's gridDim.x (the merge recomputes the split with it)
     int32_t *err;
     int32_t stages;
     int32_t window;                // > 0: attend only the last `window` keys
@@ -842,23 +843,62 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : (D =
 // beside a decode CTA and are waiting there when it finishes; the same code
 // with 512 threads, or with more registers, starts later.
 constexpr int kMergeThreads = 256;
+// Calls of at most this many sequences with fewer than 8 query heads per
+// merge CTA (the host picks 8 for 128 sequences or more): the merge
+// recomputes the split itself.  Large calls read the decode kernel's
+// metadata instead: there 1,024 merge CTAs scanning 256 lengths each beside
+// the running decode kernel slowed the GQA decode step from 0.358 to 0.361 ms,
+// while the GPT-2-shaped step gained 1-2% (0.2171 -> 0.2150 ms, fused 0.2048
+// -> 0.2007; A/B, one box).
+constexpr int kMergeScanMaxSeqs = 1024;
 
 template <int D, typename T, int kMergeHeads>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
     extern __shared__ float4 s_merge[];  // [groups][kMergeHeads * D / 4] partial sums, then [parts][heads] weights
+    __shared__ int s_scan[32];
+    __shared__ long long s_start;
+    const int s = blockIdx.x;
+    // The split of the concatenated sub-blocks into CTA ranges depends only on
+    // the call's inputs (lengths, row offsets, window, table width), which the
+    // decode kernel read after its own dependency wait.  This grid starts only
+    // once every decode CTA has passed that wait, so the inputs are final here:
+    // the split is recomputed before this kernel's wait instead of being read
+    // back from the decode kernel's metadata after it (one dependent round trip
+    // fewer on the call's path).  Every CTA still waits before it exits, so this
+    // grid never completes ahead of the decode grid.
+    const bool early = kMergeHeads < 8 && p.num_seqs <= kMergeScanMaxSeqs;
+    int64_t total = 0, start = 0, n = 0, ctas = 0;
+    if (early) {
+        int64_t carry = 0;
+        for (int s0 = 0; s0 < p.num_seqs; s0 += blockDim.x) {
+            const int t = s0 + threadIdx.x;
+            const int v = t < p.num_seqs ? decode_sub_blocks(p, t) : 0;
+            int chunk;
+            const int incl = block_scan(v, s_scan, &chunk);
+            if (t == s) s_start = carry + incl - v;
+            carry += chunk;
+        }
+        __syncthreads();
+        total = carry;
+        start = s_start;
+        n = decode_sub_blocks(p, s);
+        const int64_t want = (total + kMinSubBlocksPerCta - 1) / kMinSubBlocksPerCta;
+        ctas = want < p.grid_x ? want : p.grid_x;  // as the decode kernel takes it
+    }
     pdl_wait();
     pdl_trigger();
-    const int s = blockIdx.x;
     if (p.cu_q && p.cu_q[s + 1] - p.cu_q[s] != 1) return;
     const int64_t qrow = p.cu_q ? (int64_t)p.cu_q[s] : (int64_t)s;
     const int G = p.group, HG = p.heads_per_cta;
     const int hq = p.hkv * G;
     const int h0 = blockIdx.y * kMergeHeads;
     const int nh = min(kMergeHeads, hq - h0);
-    const int64_t total = p.ws_meta[0];
-    const int64_t ctas = p.ws_meta[1];
-    const int64_t start = p.ws_meta[2 + s];
-    const int64_t n = p.ws_meta[3 + s] - start;
+    if (!early) {
+        total = p.ws_meta[0];
+        ctas = p.ws_meta[1];
+        start = p.ws_meta[2 + s];
+        n = p.ws_meta[3 + s] - start;
+    }
     const int64_t ob = (qrow * (int64_t)hq + h0) * D;
     if (n == 0) {
         for (int i = threadIdx.x; i < nh * D; i += blockDim.x) {
@@ -1028,7 +1068,9 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     const int64_t bound = (int64_t)p.num_seqs * p.max_blocks * ((p.block_size + kSub - 1) / kSub);
     const int64_t need = (bound + kMinSubBlocksPerCta - 1) / kMinSubBlocksPerCta;
     const unsigned grid_x = (unsigned)(need < 1 ? 1 : need < pl.cmax ? need : pl.cmax);
-    st = launch_pdl(kern, dim3(grid_x, pl.num_hg), dim3(pl.threads), (size_t)pl.smem_bytes, stream, mk, mv, p);
+    DecodeParams pg = p;
+    pg.grid_x = (int32_t)grid_x;
+    st = launch_pdl(kern, dim3(grid_x, pl.num_hg), dim3(pl.threads), (size_t)pl.smem_bytes, stream, mk, mv, pg);
     if (st != PKV_OK) return st;
     // the merge reads only what the decode kernel wrote: launch it as a
     // programmatic dependent so it is scheduled while the decode kernel drains
@@ -1048,7 +1090,7 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     auto merge = mh == 8 ? decode_merge_kernel<D, T, 8> : mh == 4 ? decode_merge_kernel<D, T, 4> : decode_merge_kernel<D, T, 1>;
-    PKV_CUDA_TRY(cudaLaunchKernelEx(&cfg, merge, p));
+    PKV_CUDA_TRY(cudaLaunchKernelEx(&cfg, merge, pg));
     return PKV_OK;
 }
 
