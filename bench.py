@@ -1006,16 +1006,34 @@ def cpu_baseline_prefill(m, budget_s: float) -> dict:
                       f"{dt:.1f} s; one core: the last 64 rows of one chunk ({dt_1:.1f} s); binary64 C oracle"}
 
 
-def time_parts(parts, iters, warmup, clk, before=None):
+def time_parts(parts, iters, warmup, clk, before=None, clean=False):
     """CUDA-event time (ms) of each callable of ``parts`` per iteration, on the
     current stream; ``before`` (an L2 flush) runs outside the events.  Returns
-    the [iters][parts] times and the clock summary of the timed window."""
+    the [iters][parts] times and the clock summary of the timed window; with
+    ``clean`` (no ``before``) also the mean time of one iteration from a first
+    pass of ``iters`` iterations between one start and one end event (the
+    launches chained as a caller issues them: an event recorded between two
+    launches serialises them), whose clocks are then the ones returned."""
     for _ in range(warmup):
         if before is not None:
             before()
         for f in parts:
             f()
     torch.cuda.synchronize()
+    clean_ms = None
+    if clean and before is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        a.record()
+        for _ in range(iters):
+            for f in parts:
+                f()
+        b.record()
+        clk.poll_until(b)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        clean_ms = a.elapsed_time(b) / iters
+        ck_clean = clk.summary(t0, t1)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(iters)]
     end = torch.cuda.Event()
     t0 = time.perf_counter()
@@ -1030,13 +1048,21 @@ def time_parts(parts, iters, warmup, clk, before=None):
     clk.poll_until(end)
     torch.cuda.synchronize()
     t1 = time.perf_counter()
-    return [[e[j].elapsed_time(e[j + 1]) for j in range(len(parts))] for e in ev], clk.summary(t0, t1)
+    times = [[e[j].elapsed_time(e[j + 1]) for j in range(len(parts))] for e in ev]
+    if clean_ms is not None:
+        return times, ck_clean, clean_ms
+    return times, clk.summary(t0, t1)
 
 
 def _hbm_roofline(bytes_, ms, peak, kernel):
     a = bytes_ / (ms * 1e-3) / 1e9
     return {"bound": "hbm", "kernel": kernel, "achieved": a, "peak": peak, "unit": "GB/s", "frac": a / peak,
             "algorithmic_bytes_per_launch": bytes_, "launch_ms_median": ms}
+
+
+CLEAN_NOTE = ("ms_per_step: mean over the iterations timed between one start and one end event (write and "
+              "decode chained as a caller issues them); the roofline's launch time and ms_per_step_events_median "
+              "from a second pass with an event around each launch")
 
 
 def _med(xs):
@@ -1110,12 +1136,11 @@ def config_blocks(dev, iters: int, cpu_budget_s: float) -> dict:
         # 4: long / skewed contexts 1k .. 128k, split-K over every CTA
         w = W.long_skewed_decode()
         st = DecodeStep(w, dev)
-        ms, ck = time_parts([st.write, st.decode], iters, wu, clk)
+        ms, ck, step = time_parts([st.write, st.decode], iters, wu, clk, clean=True)
         dec_b, wr_b = st.bytes()
-        step = _med([a + b for a, b in ms])
         out["skew"] = {
-            "workload": w.name, "iters": iters, "ms_per_step": step,
-            "ms_per_step_mean": float(np.mean([a + b for a, b in ms])), "tokens_per_s": w.batch / (step * 1e-3),
+            "workload": w.name, "iters": iters, "ms_per_step": step, "timed_as": CLEAN_NOTE,
+            "ms_per_step_events_median": _med([a + b for a, b in ms]), "tokens_per_s": w.batch / (step * 1e-3),
             "GB_per_s": (dec_b + wr_b) / (step * 1e-3) / 1e9, "l2": "1.07 GB of K/V per step, no flush",
             "roofline": _hbm_roofline(dec_b, _med([b for _, b in ms]), hbm, "pkv_attn_decode (split-K + merge)"),
             "clocks": ck, "cpu_baseline": cpu_baseline_decode(w, cpu_budget_s, cpu_budget_s / 2)}
@@ -1127,12 +1152,11 @@ def config_blocks(dev, iters: int, cpu_budget_s: float) -> dict:
         # GQA 32/8 over an int8 cache (codes + per-block-per-head scales)
         w = W.gqa_decode()
         st = DecodeStepInt8(w, dev)
-        ms, ck = time_parts([st.write, st.decode], iters, wu, clk)
+        ms, ck, step = time_parts([st.write, st.decode], iters, wu, clk, clean=True)
         dec_b, wr_b = st.bytes()
-        step = _med([a + b for a, b in ms])
         out["gqa_int8"] = {
-            "workload": w.name + "_int8", "iters": iters, "ms_per_step": step,
-            "ms_per_step_mean": float(np.mean([a + b for a, b in ms])), "tokens_per_s": w.batch / (step * 1e-3),
+            "workload": w.name + "_int8", "iters": iters, "ms_per_step": step, "timed_as": CLEAN_NOTE,
+            "ms_per_step_events_median": _med([a + b for a, b in ms]), "tokens_per_s": w.batch / (step * 1e-3),
             "GB_per_s": (dec_b + wr_b) / (step * 1e-3) / 1e9, "l2": "1.21 GB of codes per step, no flush",
             "roofline": _hbm_roofline(dec_b, _med([b for _, b in ms]), hbm, "pkv_attn_decode_int8 (split-K + merge)"),
             "clocks": ck, "cpu_baseline": cpu_baseline_decode(w, cpu_budget_s, cpu_budget_s / 2, int8=True)}
@@ -1146,13 +1170,13 @@ def config_blocks(dev, iters: int, cpu_budget_s: float) -> dict:
         w = W.gqa_decode()
         st = DecodeStep(w, dev)
         st.window = 1024
-        ms, ck = time_parts([st.write, st.decode], iters, wu, clk)
+        ms, ck, step = time_parts([st.write, st.decode], iters, wu, clk, clean=True)
         dec_b, wr_b = st.bytes()
-        step = _med([a + b for a, b in ms])
         kept = sum(windowed(w.lengths, st.window)) * kv_bytes_per_token(w.num_kv_heads, w.head_dim, 2)
         out["window"] = {
             "workload": w.name + "_window1024", "iters": iters, "window": st.window, "ms_per_step": step,
-            "ms_per_step_mean": float(np.mean([a + b for a, b in ms])), "tokens_per_s": w.batch / (step * 1e-3),
+            "timed_as": CLEAN_NOTE, "ms_per_step_events_median": _med([a + b for a, b in ms]),
+            "tokens_per_s": w.batch / (step * 1e-3),
             "GB_per_s": (dec_b + wr_b) / (step * 1e-3) / 1e9,
             "l2": "%.2f GB of K/V in the windows per step, no flush" % (kept / 1e9),
             "roofline": _hbm_roofline(dec_b, _med([b for _, b in ms]), hbm, "pkv_attn_decode_window (split-K + merge)"),
