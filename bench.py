@@ -706,7 +706,7 @@ def reference_arm(args, rank: int):
 # ---------------------------------------------------------------------------
 
 class MixedStep:
-    """GQA 32/8, D 128, fp16, block_size 32.  Step 1: a 2048-token prefix
+    """GQA 32/8, D 128, fp16 (or ``dtype``), block_size 32.  Step 1: a 2048-token prefix
     shared (whole blocks) by 16 prefill chunks of 512 rows and 240 decode
     sequences with total contexts U[256, 8192]; 8432 new rows written, then one
     packed varlen call.  Step 2: 32 decode sequences fork to width 4, each beam
@@ -714,10 +714,10 @@ class MixedStep:
     write, decode over the 128 beams.  Slots, tables and pairs come from the
     product allocator, set up once; the timed steps replay them."""
 
-    def __init__(self, dev: torch.device):
+    def __init__(self, dev: torch.device, dtype: str = "f16"):
         import pagedattention_decode_gb300 as P
         self.P, self.dev = P, dev
-        bs, hq, hkv, d, self.dtype = 32, 32, 8, 128, "f16"
+        bs, hq, hkv, d, self.dtype = 32, 32, 8, 128, dtype
         self.bs, self.hq, self.hkv, self.d = bs, hq, hkv, d
         self.scale = 1.0 / math.sqrt(d)
         g = W.generator(5)

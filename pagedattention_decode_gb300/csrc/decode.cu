@@ -176,9 +176,10 @@ __device__ __forceinline__ uint32_t i8_pair<__half>(uint32_t x, uint32_t sel) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// fp16 codes + 1152 (1024 + 128 + code, exact) without the subtraction: the
-// decode kernel takes the bias out of the scores (1152 * sum of q) and out of
-// O (1152 * sum of the P fed to the MMA) instead.
+// fp16 codes + 1152 (1024 + 128 + code, exact) without the subtraction, for
+// the K codes: the decode kernel takes the bias out of the scores (1152 * sum
+// of q), which costs them ~1e-4 of relative precision.  V codes enter P V
+// without the bias (i8_pair): there it would sit in the fp32 accumulator of O.
 __device__ __forceinline__ uint32_t i8_pair_biased(uint32_t x, uint32_t sel) {
     return __byte_perm(x, 0x64646464u, sel);
 }
@@ -503,9 +504,9 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : (D =
             }
         }
         float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
-        // int8 codes of an fp16 cache enter the MMAs as code + 1152 (see i8_pair_biased)
+        // int8 K codes of an fp16 cache enter the score MMAs as code + 1152 (see i8_pair_biased)
         constexpr bool BIAS = I8 && IsHalf<T>::value;
-        float qsA = 0.f, qsB = 0.f, pvA = 0.f, pvB = 0.f;
+        float qsA = 0.f, qsB = 0.f;
         if constexpr (BIAS) {
             // sum of q over head_dim for heads hA, hB: lane 4g + t4 holds a quarter of head g
             float qs = 0.f;
@@ -641,10 +642,6 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : (D =
             // P as the B operand (16 tokens x 8 heads), hi and lo 16-bit parts
             // (int8: P is scaled by the block's V scale, so the codes multiply directly)
             const float q0 = p0 * vsc, q1 = p1 * vsc, q2 = p2 * vsc, q3 = p3 * vsc;
-            if constexpr (BIAS) {  // the P fed to P V, per head, rescaled as O is
-                pvA = pvA * aA + (q0 + q2);
-                pvB = pvB * aB + (q1 + q3);
-            }
             const uint32_t h01 = pack2<T>(q0, q1), h23 = pack2<T>(q2, q3);
             const float2 r01 = unpack2<T>(h01), r23 = unpack2<T>(h23);
             const uint32_t l01 = pack2<T>(q0 - r01.x, q1 - r01.y), l23 = pack2<T>(q2 - r23.x, q3 - r23.y);
@@ -668,18 +665,16 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : (D =
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
                             const uint32_t lo = r[2 * u] ^ 0x80808080u, hi = r[2 * u + 1] ^ 0x80808080u;
+                            // the signed codes themselves (no 1152 bias): O accumulates
+                            // only the signal, so the fp32 accumulator keeps its
+                            // precision on long sequences (with the bias it held
+                            // ~15x the signal, and 2-4k-token rows of the GQA int8
+                            // workload missed the binary64 oracle by up to 6.5e-3)
                             uint32_t a[4];
-                            if constexpr (BIAS) {
-                                a[0] = i8_pair_biased(lo, 0x4240u);
-                                a[1] = i8_pair_biased(lo, 0x4341u);
-                                a[2] = i8_pair_biased(hi, 0x4240u);
-                                a[3] = i8_pair_biased(hi, 0x4341u);
-                            } else {
-                                a[0] = i8_pair<T>(lo, 0x4240u);
-                                a[1] = i8_pair<T>(lo, 0x4341u);
-                                a[2] = i8_pair<T>(hi, 0x4240u);
-                                a[3] = i8_pair<T>(hi, 0x4341u);
-                            }
+                            a[0] = i8_pair<T>(lo, 0x4240u);
+                            a[1] = i8_pair<T>(lo, 0x4341u);
+                            a[2] = i8_pair<T>(hi, 0x4240u);
+                            a[3] = i8_pair<T>(hi, 0x4341u);
                             mma_16816<T>(o[2 * m2 + u], a, bh0, bh1);
                             if constexpr (decltype(lo_pass)::value) mma_16816<T>(o[2 * m2 + u], a, bl0, bl1);
                         }
@@ -750,21 +745,6 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : (D =
         for (int off = 4; off < 32; off <<= 1) {
             lA += __shfl_xor_sync(0xffffffffu, lA, off);
             lB += __shfl_xor_sync(0xffffffffu, lB, off);
-        }
-        if constexpr (BIAS) {
-            // O holds sum_t P_t (code_t + 1152): take 1152 * sum_t P_t out
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                pvA += __shfl_xor_sync(0xffffffffu, pvA, off);
-                pvB += __shfl_xor_sync(0xffffffffu, pvB, off);
-            }
-#pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-                o[mt][0] = fmaf(-1152.f, pvA, o[mt][0]);
-                o[mt][2] = fmaf(-1152.f, pvA, o[mt][2]);
-                o[mt][1] = fmaf(-1152.f, pvB, o[mt][1]);
-                o[mt][3] = fmaf(-1152.f, pvB, o[mt][3]);
-            }
         }
         const bool complete = (sb == 0 && b1 == n_s);
         if (complete) {

@@ -21,12 +21,14 @@ from tests.cases import Subset, assert_close
 pytestmark = pytest.mark.gpu
 
 
-def test_mixed_step_full_size_every_row():
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_mixed_step_full_size_every_row(dtype):
     """Every output row of both steps: the 16 x 512 prefill rows and 240
-    decode rows of the packed step, then all 128 beams after the split."""
+    decode rows of the packed step, then all 128 beams after the split (bf16:
+    the same step over a bf16 cache, P entering P V as a hi + lo pair)."""
     import bench
     dev = torch.device("cuda", torch.cuda.current_device())
-    m = bench.MixedStep(dev)
+    m = bench.MixedStep(dev, dtype)
     s1, s2 = m.s1, m.s2
     tab1, tab2 = s1["tables"].cpu(), s2["tables"].cpu()
     rows1 = [tab1[i].tolist() for i in range(tab1.shape[0])]
@@ -47,15 +49,15 @@ def test_mixed_step_full_size_every_row():
     # oracle replay of step 1: the writes, then the whole packed call (causal rows)
     sub.write(slots1, k1, v1)
     cu = s1["cu"].cpu().numpy()
-    want1 = sub.attend(s1["q"].cpu(), [sub.table(r) for r in rows1], m.s1_lens_host, m.scale, "f16", cu_q=cu)
+    want1 = sub.attend(s1["q"].cpu(), [sub.table(r) for r in rows1], m.s1_lens_host, m.scale, dtype, cu_q=cu)
     n_pf = m.nchunk * m.chunk
-    assert_close(out1[:n_pf], want1[:n_pf], what="step 1 prefill rows")
-    assert_close(out1[n_pf:], want1[n_pf:], what="step 1 decode rows")
+    assert_close(out1[:n_pf], want1[:n_pf], what=f"step 1 prefill rows ({dtype})")
+    assert_close(out1[n_pf:], want1[n_pf:], what=f"step 1 decode rows ({dtype})")
     # oracle replay of step 2: copies, writes, decode of every beam
     sub.copy(pairs2)
     sub.write(slots2, k2, v2)
-    want2 = sub.attend(s2["q"].cpu(), [sub.table(r) for r in rows2], m.s2_lens_host, m.scale, "f16")
-    assert_close(out2, want2, what="step 2 beams")
+    want2 = sub.attend(s2["q"].cpu(), [sub.table(r) for r in rows2], m.s2_lens_host, m.scale, dtype)
+    assert_close(out2, want2, what=f"step 2 beams ({dtype})")
 
 
 def test_gpt2_shaped_twelve_layers_every_sequence():

@@ -128,3 +128,41 @@ def test_int8_decode_long_split_and_16bit_out():
     torch.cuda.synchronize()
     want = oracle.paged_attention_int8(q, "f16", kq, vq, ks, vs, tables, L, 0.088)
     assert_close(out, want, what="int8 long")
+
+
+def test_int8_full_size_workload_every_sequence():
+    """The int8 row at the bench's shapes (GQA 32/8, 256 sequences of 512-4096
+    tokens, random codes and per-block-per-head scales as the bench makes
+    them), launched as the bench launches it: every sequence against the int8
+    oracle, those cut over several CTAs (merged) included."""
+    w = W.gqa_decode()
+    dev = "cuda"
+    B, hq, hkv, d, bs = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed * 100 + 77)
+    shape = (w.num_blocks, bs, hkv, d)
+    kq = torch.randint(-127, 128, shape, generator=g, dtype=torch.int8, device=dev)
+    vq = torch.randint(-127, 128, shape, generator=g, dtype=torch.int8, device=dev)
+    ks = torch.rand((w.num_blocks, hkv), generator=g, device=dev) * 0.03 + 0.01
+    vs = torch.rand((w.num_blocks, hkv), generator=g, device=dev) * 0.03 + 0.01
+    gh = W.generator(w.seed)
+    q = W.normal(gh, (B, hq, d), w.sigma, w.dtype)
+    tables, _ = W.scattered_tables(gh, w.lengths, bs, w.num_blocks)
+    lens = torch.tensor(w.lengths, dtype=torch.int32)
+    # host copy of the blocks the sequences use, ids renumbered (before any kernel of ours runs)
+    ids = sorted({int(b) for b in tables.flatten().tolist() if b >= 0})
+    local = {b: i for i, b in enumerate(ids)}
+    idx = torch.tensor(ids, dtype=torch.long, device=dev)
+    kq_h, vq_h = kq[idx].cpu().numpy(), vq[idx].cpu().numpy()
+    ks_h, vs_h = ks[idx].cpu().numpy(), vs[idx].cpu().numpy()
+    tab_l = np.full(tables.shape, -1, np.int32)
+    for i in range(B):
+        row = [local[int(b)] for b in tables[i].tolist() if b >= 0]
+        tab_l[i, :len(row)] = row
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = P.attn_decode_int8(q.to(dev), kq, vq, ks, vs, tables.to(dev), lens.to(dev), w.scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    del kq, vq
+    want = oracle.paged_attention_int8(q, w.dtype, kq_h, vq_h, ks_h, vs_h, tab_l, lens.numpy(), w.scale)
+    assert_close(out, want, what=w.name + " int8")
