@@ -9,7 +9,7 @@ import torch
 import oracle
 import pagedattention_decode_gb300 as P
 import workloads as W
-from tests.cases import assert_close, decode_case
+from tests.cases import Subset, assert_close, decode_case
 
 pytestmark = pytest.mark.gpu
 
@@ -113,3 +113,37 @@ def test_append_bad_block_is_flagged_and_not_written():
     changed = (_bits(k1) != before).view(-1, 2 * 64).any(dim=1).nonzero().view(-1).tolist()
     assert changed == [slot0] or changed == []
     assert torch.equal(k1.view(-1, 2, 64)[slot0].cpu(), kn[0])
+
+
+def test_append_full_size_workload_every_sequence():
+    """The GQA 32/8 workload (256 sequences of 512-4096 tokens) with each
+    sequence's new row written by the decode kernel: outputs and pools bit
+    for bit those of pkv_write_kv + pkv_attn_decode, and every output within
+    2e-3 of the oracle's slot write followed by binary64 attention."""
+    w = W.gqa_decode()
+    dev = "cuda"
+    bs = w.block_size
+    shape = (w.num_blocks, bs, w.num_kv_heads, w.head_dim)
+    k1 = W.normal_device(w.seed * 10 + 1, shape, w.sigma, w.dtype, dev)
+    v1 = W.normal_device(w.seed * 10 + 2, shape, w.sigma, w.dtype, dev)
+    g = W.generator(w.seed)
+    q = W.normal(g, (w.batch, w.num_q_heads, w.head_dim), w.sigma, w.dtype)
+    tables, _ = W.scattered_tables(g, w.lengths, bs, w.num_blocks)
+    kn = W.normal(g, (w.batch, w.num_kv_heads, w.head_dim), w.sigma, w.dtype)
+    vn = W.normal(g, (w.batch, w.num_kv_heads, w.head_dim), w.sigma, w.dtype)
+    lens = torch.tensor(w.lengths, dtype=torch.int32)
+    slots = [int(tables[i, (L - 1) // bs]) * bs + (L - 1) % bs for i, L in enumerate(w.lengths)]
+    rows = [tables[i].tolist() for i in range(w.batch)]
+    sub = Subset(k1, v1, rows)   # before any kernel of ours runs
+    k2, v2 = k1.clone(), v1.clone()
+    qd, td, ld = q.to(dev), tables.to(dev), lens.to(dev)
+    out1 = P.attn_decode(qd, k1, v1, td, ld, w.scale, k_new=kn.to(dev), v_new=vn.to(dev))
+    P.write_kv(kn.to(dev), vn.to(dev), torch.tensor(slots, dtype=torch.int64, device=dev), k2, v2)
+    out2 = P.attn_decode(qd, k2, v2, td, ld, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)
+    assert torch.equal(_bits(k1), _bits(k2)) and torch.equal(_bits(v1), _bits(v2))
+    del k1, v1, k2, v2
+    sub.write(slots, kn, vn)
+    want = sub.attend(q, [sub.table(r) for r in rows], w.lengths, w.scale, w.dtype)
+    assert_close(out1, want, what=w.name + " append")

@@ -130,11 +130,13 @@ def test_int8_decode_long_split_and_16bit_out():
     assert_close(out, want, what="int8 long")
 
 
-def test_int8_full_size_workload_every_sequence():
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_int8_full_size_workload_every_sequence(dtype):
     """The int8 row at the bench's shapes (GQA 32/8, 256 sequences of 512-4096
     tokens, random codes and per-block-per-head scales as the bench makes
     them), launched as the bench launches it: every sequence against the int8
-    oracle, those cut over several CTAs (merged) included."""
+    oracle, those cut over several CTAs (merged) included (bf16: the same
+    codes with bf16 queries)."""
     w = W.gqa_decode()
     dev = "cuda"
     B, hq, hkv, d, bs = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
@@ -146,7 +148,7 @@ def test_int8_full_size_workload_every_sequence():
     ks = torch.rand((w.num_blocks, hkv), generator=g, device=dev) * 0.03 + 0.01
     vs = torch.rand((w.num_blocks, hkv), generator=g, device=dev) * 0.03 + 0.01
     gh = W.generator(w.seed)
-    q = W.normal(gh, (B, hq, d), w.sigma, w.dtype)
+    q = W.normal(gh, (B, hq, d), w.sigma, dtype)
     tables, _ = W.scattered_tables(gh, w.lengths, bs, w.num_blocks)
     lens = torch.tensor(w.lengths, dtype=torch.int32)
     # host copy of the blocks the sequences use, ids renumbered (before any kernel of ours runs)
@@ -164,5 +166,5 @@ def test_int8_full_size_workload_every_sequence():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     del kq, vq
-    want = oracle.paged_attention_int8(q, w.dtype, kq_h, vq_h, ks_h, vs_h, tab_l, lens.numpy(), w.scale)
-    assert_close(out, want, what=w.name + " int8")
+    want = oracle.paged_attention_int8(q, dtype, kq_h, vq_h, ks_h, vs_h, tab_l, lens.numpy(), w.scale)
+    assert_close(out, want, what=f"{w.name} int8 {dtype}")
