@@ -60,6 +60,33 @@ def test_mixed_step_full_size_every_row(dtype):
     assert_close(out2, want2, what=f"step 2 beams ({dtype})")
 
 
+def test_mixed_step_full_size_window_every_row():
+    """Step 1 of the mixed workload with a 1,024-key sliding window: the
+    prefill chunks skip the tiles before each row's window and mask inside
+    the first tile they read; every row against the oracle."""
+    import bench
+    dev = torch.device("cuda", torch.cuda.current_device())
+    m = bench.MixedStep(dev)
+    s1 = m.s1
+    tab1 = s1["tables"].cpu()
+    rows1 = [tab1[i].tolist() for i in range(tab1.shape[0])]
+    sub = Subset(m.k_cache, m.v_cache, rows1)   # before any of our kernels ran
+    k1, v1, slots1 = s1["k"].cpu(), s1["v"].cpu(), s1["slots"].cpu().tolist()
+    window = 1024
+    P.write_kv(s1["k"], s1["v"], s1["slots"], m.k_cache, m.v_cache, err=m.err)
+    out = P.attn_varlen(s1["q"], m.k_cache, m.v_cache, s1["tables"], s1["cu"], s1["lens"], s1["max_q"], m.scale,
+                        workspace=m.ws, err=m.err, window=window)
+    torch.cuda.synchronize()
+    assert int(m.err.item()) == 0
+    sub.write(slots1, k1, v1)
+    cu = s1["cu"].cpu().numpy()
+    want = sub.attend(s1["q"].cpu(), [sub.table(r) for r in rows1], m.s1_lens_host, m.scale, "f16", cu_q=cu,
+                      window=window)
+    n_pf = m.nchunk * m.chunk
+    assert_close(out[:n_pf], want[:n_pf], what="window prefill rows")
+    assert_close(out[n_pf:], want[n_pf:], what="window decode rows")
+
+
 def test_gpt2_shaped_twelve_layers_every_sequence():
     w = W.gpt2_decode()
     dev = "cuda"
