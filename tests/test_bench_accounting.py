@@ -40,3 +40,17 @@ def test_split_records_brute_force():
                     want += len(cs)
                 start += k
         assert bench.split_records(lens, ctas_max) == want
+
+
+def test_window_keeps_each_sequences_last_keys():
+    """A window of w keys counts min(L, w) keys per sequence (all of them when
+    there is no window), as the windowed decode attends them."""
+    lens = [0, 1, 15, 1023, 1024, 1025, 4096]
+    assert bench.windowed(lens, 0) == lens
+    assert bench.windowed(lens, 1024) == [0, 1, 15, 1023, 1024, 1024, 1024]
+    assert bench.windowed(lens, 1) == [0, 1, 1, 1, 1, 1, 1]
+    # the windowed decode's bytes are those of a call over the kept lengths
+    kept = bench.windowed(lens, 1024)
+    assert bench.decode_bytes(kept, 32, 8, 128, 2, 4, 152) == bench.decode_bytes(
+        [min(L, 1024) for L in lens], 32, 8, 128, 2, 4, 152)
+    assert sum(kept) * bench.kv_bytes_per_token(8, 128, 2) < sum(lens) * bench.kv_bytes_per_token(8, 128, 2)
