@@ -79,6 +79,8 @@ def split_records(lengths, ctas_max: int, sub: int = 16, min_per_cta: int = 4) -
     total = sum(n)
     if total == 0:
         return 0
+    if len(lengths) <= 32 and total <= 64 and len(lengths) <= ctas_max:
+        return 0  # a CTA per sequence, each taking its sequence whole
     ctas = min(ctas_max, -(-total // min_per_cta))
     recs, start = 0, 0
     for k in n:

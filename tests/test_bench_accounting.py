@@ -26,7 +26,8 @@ def test_split_records_brute_force():
         n = [-(-L // 16) for L in lens]
         total = sum(n)
         want = 0
-        if total:
+        whole = len(lens) <= 32 and total <= 64 and len(lens) <= ctas_max  # a CTA per sequence
+        if total and not whole:
             ctas = min(ctas_max, -(-total // 4))
             owner = []
             for c in range(ctas):

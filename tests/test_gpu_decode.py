@@ -147,6 +147,20 @@ def test_gqa_mapping_contiguous_groups():
     assert torch.allclose(got[0].cpu(), want, atol=1e-6)
 
 
+@pytest.mark.parametrize("lens", [[16, 32] * 16,            # 32 sequences, 48 sub-blocks: whole
+                                  [32] * 31 + [33],         # 32 sequences, exactly 64 + 1: even split
+                                  [16] * 40,                # 40 sequences, 40 sub-blocks: even split
+                                  [32] * 32,                # 32 sequences, exactly 64: whole
+                                  [5, 40]])                 # the even split would cut the second
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (12, 12, 64)])
+def test_small_calls_one_cta_per_sequence(lens, hq, hkv, d):
+    """Calls of at most 32 sequences and 64 sub-blocks give each sequence a
+    CTA of its own (no cut, nothing to merge); just past either bound the
+    even split takes over.  Both sides of the bounds against the oracle."""
+    case = decode_case(97 + len(lens) + d, lens, hq, hkv, d, 16, "f16")
+    assert_close(run(case), case.oracle(), what=f"{len(lens)} sequences, {sum(-(-L // 16) for L in lens)} sub-blocks")
+
+
 @pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (12, 12, 64)])
 @pytest.mark.parametrize("window", [0, 16])
 def test_every_sequence_empty(hq, hkv, d, window):
