@@ -16,9 +16,10 @@
 //    leaves (running max, running sum, unnormalised output) records in the
 //    workspace that decode_merge_kernel combines.  Balance is exact whatever
 //    the length mix.  A call of at most 32 sequences and 64 sub-blocks takes
-//    a CTA per sequence instead (no cut, nothing to merge): the tiny MHA call
-//    went from 22.0 to 16.6-17.9 us per write + decode step, its decode call
-//    from 15.4 to 10.2-11.3 us (A/B, L2 flushed).
+//    a CTA per sequence instead (no cut, nothing to merge, and when the
+//    tables' capacity already guarantees the bounds no merge launch): the
+//    tiny MHA call went from 22.0 to 16.3-16.6 us per write + decode step
+//    (A/B, L2 flushed).
 //  * Data movement: one producer warp walks the block tables and issues two
 //    TMA tensor loads per 16-token sub-block, K and V, into a ring of
 //    shared-memory stages guarded by mbarriers.  Each load is one box of 16
@@ -315,6 +316,22 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : (D =
         p.ws_meta[0] = (int)total;
         p.ws_meta[1] = ctas;
         p.ws_meta[2 + p.num_seqs] = (int)total;
+    }
+    if (whole && lo >= hi && blockIdx.x < ctas) {
+        // an empty decode row of a call whose merge is not launched: its zero
+        // rows (this head group's query heads) come from here
+        const int s = blockIdx.x;
+        if (!p.cu_q || p.cu_q[s + 1] - p.cu_q[s] == 1) {
+            const int64_t qrow = p.cu_q ? (int64_t)p.cu_q[s] : (int64_t)s;
+            const int nq = HG * p.group;
+            const int64_t ob = (qrow * (int64_t)(p.hkv * p.group) + (int64_t)hg * nq) * D;
+            for (int i = tid; i < nq * D; i += blockDim.x) {
+                if (p.out_f32)
+                    static_cast<float *>(p.out)[ob + i] = 0.f;
+                else
+                    static_cast<T *>(p.out)[ob + i] = static_cast<T>(0.f);
+            }
+        }
     }
     if (blockIdx.x >= ctas || lo >= hi) return;
 
@@ -1082,6 +1099,11 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     pg.grid_x = (int32_t)grid_x;
     st = launch_pdl(kern, dim3(grid_x, pl.num_hg), dim3(pl.threads), (size_t)pl.smem_bytes, stream, mk, mv, pg);
     if (st != PKV_OK) return st;
+    // a call the small-call split surely covers (total <= bound, grid = a CTA
+    // per sequence) cuts no sequence, and its empty rows are written by the
+    // decode kernel: no merge
+    if (p.num_seqs <= kWholeSeqMaxSeqs && bound <= kWholeSeqMaxSubBlocks && (int64_t)p.num_seqs <= (int64_t)grid_x)
+        return PKV_OK;
     // the merge reads only what the decode kernel wrote: launch it as a
     // programmatic dependent so it is scheduled while the decode kernel drains
     // many sequences: 8 query heads per merge CTA (fewer, mostly idle, CTAs);

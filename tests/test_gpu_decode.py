@@ -151,7 +151,7 @@ def test_gqa_mapping_contiguous_groups():
                                   [32] * 31 + [33],         # 32 sequences, exactly 64 + 1: even split
                                   [16] * 40,                # 40 sequences, 40 sub-blocks: even split
                                   [32] * 32,                # 32 sequences, exactly 64: whole
-                                  [5, 40]])                 # the even split would cut the second
+                                  [5, 0, 40]])              # the even split would cut the third
 @pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (12, 12, 64)])
 def test_small_calls_one_cta_per_sequence(lens, hq, hkv, d):
     """Calls of at most 32 sequences and 64 sub-blocks give each sequence a
