@@ -60,3 +60,18 @@ def test_host_side_argument_checks_need_no_gpu():
     assert L.pkv_check_copy_pairs(pairs, 2, 8) == 0
     pairs = (ctypes.c_int64 * 2)(1, 9)
     assert L.pkv_check_copy_pairs(pairs, 1, 8) == 4
+
+
+def test_varlen_with_no_query_rows_is_a_host_side_no_op():
+    """total_q == 0 (every sequence's row set empty): the call returns PKV_OK
+    with NULL q / out before any device work (it needs no GPU); a negative
+    total_q is refused."""
+    from pagedattention_decode_gb300 import _native
+    L = _native.lib()
+    c = _native.PkvCache(16, 32, 8, 16, 2, 64, 0)  # fp16 pool geometry; never dereferenced here
+    st = L.pkv_attn_varlen(None, 8 * 64, ctypes.byref(c), None, 1, None, None, 3, 0, 0, 8, 0.125, 1, None, 2,
+                           None, 0, None, None)
+    assert st == 0, L.pkv_last_error()
+    st = L.pkv_attn_varlen(None, 8 * 64, ctypes.byref(c), None, 1, None, None, 3, -1, 0, 8, 0.125, 1, None, 2,
+                           None, 0, None, None)
+    assert st == 1
