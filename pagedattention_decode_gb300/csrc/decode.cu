@@ -82,6 +82,11 @@ constexpr int kMinSubBlocksPerCta = 4;
 // so no sequence is cut and the merge has nothing to combine.
 constexpr int kWholeSeqMaxSeqs = 32;
 constexpr int kWholeSeqMaxSubBlocks = 64;
+// The one test of that split, shared by the host (with its bound on the
+// sub-blocks), the decode kernel and the merge (with the actual count).
+__host__ __device__ __forceinline__ bool whole_seq_split(int64_t sub_blocks, int64_t num_seqs, int64_t grid_x) {
+    return sub_blocks <= kWholeSeqMaxSubBlocks && num_seqs <= kWholeSeqMaxSeqs && num_seqs <= grid_x;
+}
 
 struct DecodeParams {
     const void *q;
@@ -267,8 +272,7 @@ __global__ void __launch_bounds__(cta_threads<D, I8>(), I8 ? kI8CtasPerSm : (D =
         }
         total += chunk;
     }
-    const bool whole = total <= kWholeSeqMaxSubBlocks && p.num_seqs <= kWholeSeqMaxSeqs &&
-                       p.num_seqs <= (int)gridDim.x;
+    const bool whole = whole_seq_split(total, p.num_seqs, gridDim.x);
     const int64_t want = (total + kMinSubBlocksPerCta - 1) / kMinSubBlocksPerCta;
     const int ctas = whole ? p.num_seqs : (int)(want < gridDim.x ? want : gridDim.x);
     if (blockIdx.x >= ctas && !meta_cta) return;
@@ -904,7 +908,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
         n = decode_sub_blocks(p, s);
         const int64_t want = (total + kMinSubBlocksPerCta - 1) / kMinSubBlocksPerCta;
         ctas = want < p.grid_x ? want : p.grid_x;  // as the decode kernel takes it
-        whole = total <= kWholeSeqMaxSubBlocks && p.num_seqs <= kWholeSeqMaxSeqs && p.num_seqs <= p.grid_x;
+        whole = whole_seq_split(total, p.num_seqs, p.grid_x);
     }
     pdl_wait();
     pdl_trigger();
@@ -1092,9 +1096,7 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     unsigned grid_x = (unsigned)(need < 1 ? 1 : need < pl.cmax ? need : pl.cmax);
     // a call this small even at its tables' capacity gets a CTA per sequence,
     // each taking its sequence whole (the kernels check the same bounds)
-    if (p.num_seqs <= kWholeSeqMaxSeqs && bound <= kWholeSeqMaxSubBlocks && (unsigned)p.num_seqs > grid_x &&
-        p.num_seqs <= pl.cmax)
-        grid_x = (unsigned)p.num_seqs;
+    if (whole_seq_split(bound, p.num_seqs, pl.cmax) && (unsigned)p.num_seqs > grid_x) grid_x = (unsigned)p.num_seqs;
     DecodeParams pg = p;
     pg.grid_x = (int32_t)grid_x;
     st = launch_pdl(kern, dim3(grid_x, pl.num_hg), dim3(pl.threads), (size_t)pl.smem_bytes, stream, mk, mv, pg);
@@ -1102,8 +1104,7 @@ static pkv_status launch_decode_t(const CUtensorMap &mk, const CUtensorMap &mv, 
     // a call the small-call split surely covers (total <= bound, grid = a CTA
     // per sequence) cuts no sequence, and its empty rows are written by the
     // decode kernel: no merge
-    if (p.num_seqs <= kWholeSeqMaxSeqs && bound <= kWholeSeqMaxSubBlocks && (int64_t)p.num_seqs <= (int64_t)grid_x)
-        return PKV_OK;
+    if (whole_seq_split(bound, p.num_seqs, grid_x)) return PKV_OK;
     // the merge reads only what the decode kernel wrote: launch it as a
     // programmatic dependent so it is scheduled while the decode kernel drains
     // many sequences: 8 query heads per merge CTA (fewer, mostly idle, CTAs);
